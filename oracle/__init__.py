@@ -1,0 +1,126 @@
+"""fp64 CPU oracle for the Kimi Delta Attention forward pass.
+
+TEST INFRASTRUCTURE.  Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline
+leg of ``bench.py`` import this package.  The CUDA library never calls it and shares no
+code with it: ``kda_oracle.c`` is a plain C restatement of the token recurrence
+(Tokamax "chunk_kda_fwd_design_doc", Appendix 9.1.2, Eq. (1)) and of the chunkwise form
+(same document, 9.1.3-9.1.6, Eq. (6)-(9)).
+
+Every function here is pinned by ``tests/pins.py``; ``tests/test_oracle_mutants.py``
+plants single mistakes in a copy of the C source and checks that a pin catches each.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(HERE, "kda_oracle.c")
+LIBRARY = os.path.join(HERE, "libkda_oracle.so")
+
+# -ffp-contract=off: no fused multiply-add contraction, so x86 and Arm hosts
+# evaluate the same expressions in the same fp64 operations.
+CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-ffp-contract=off"]
+
+
+def build_oracle(source: str = SOURCE, output: str = LIBRARY, force: bool = False) -> str:
+    """Compile the C oracle with gcc into a shared library and return its path."""
+    if (not force and os.path.exists(output)
+            and os.path.getmtime(output) >= os.path.getmtime(source)):
+        return output
+    cmd = ["gcc", *CFLAGS, "-I", HERE, "-o", output, source, "-lm"]
+    subprocess.run(cmd, check=True, capture_output=True, text=True)
+    return output
+
+
+def _f64(x) -> np.ndarray:
+    """Exact widening of an input tensor (bf16/fp32/fp64 torch or numpy) to fp64."""
+    if x is None:
+        return None
+    if hasattr(x, "detach"):  # torch tensor: bf16 -> fp32 is exact, numpy has no bf16
+        x = x.detach().to("cpu")
+        if str(x.dtype) == "torch.bfloat16":
+            x = x.float()
+        x = x.numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a: Optional[np.ndarray], ctype=ctypes.c_double):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+class Oracle:
+    """ctypes front end of one compiled oracle library."""
+
+    def __init__(self, lib_path: Optional[str] = None):
+        self.path = lib_path or build_oracle()
+        self.lib = ctypes.CDLL(self.path)
+        dp = ctypes.POINTER(ctypes.c_double)
+        ip = ctypes.POINTER(ctypes.c_int32)
+        common = [dp, dp, dp, dp, dp, ctypes.c_double, dp, ip, ctypes.c_int,
+                  ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]
+        self.lib.kda_oracle_recurrent.argtypes = common + [dp, dp, ctypes.c_int]
+        self.lib.kda_oracle_recurrent.restype = ctypes.c_int
+        self.lib.kda_oracle_chunkwise.argtypes = common + [ctypes.c_int, dp, dp, ctypes.c_int]
+        self.lib.kda_oracle_chunkwise.restype = ctypes.c_int
+        self.threads_used = 0
+
+    def _prepare(self, q, k, v, g, beta, initial_state, cu_seqlens):
+        q, k, v, g, beta = (_f64(t) for t in (q, k, v, g, beta))
+        B, T, H, K = q.shape
+        V = v.shape[-1]
+        if cu_seqlens is not None:
+            cu = np.ascontiguousarray(np.asarray(
+                cu_seqlens.cpu().numpy() if hasattr(cu_seqlens, "cpu") else cu_seqlens,
+                dtype=np.int32))
+            N = cu.shape[0] - 1
+        else:
+            cu, N = None, B
+        s0 = _f64(initial_state)
+        o = np.empty((B, T, H, V), dtype=np.float64)
+        fin = np.empty((N, H, K, V), dtype=np.float64)
+        return q, k, v, g, beta, s0, cu, N, B, T, H, K, V, o, fin
+
+    def recurrent(self, q, k, v, g, beta, scale, initial_state=None, cu_seqlens=None,
+                  num_threads: int = 0):
+        """Token recurrence in fp64. Returns (o [B,T,H,V], final_state [N,H,K,V])."""
+        q, k, v, g, beta, s0, cu, N, B, T, H, K, V, o, fin = self._prepare(
+            q, k, v, g, beta, initial_state, cu_seqlens)
+        rc = self.lib.kda_oracle_recurrent(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(s0),
+            _ptr(cu, ctypes.c_int32), N, B, T, H, K, V, _ptr(o), _ptr(fin), int(num_threads))
+        if rc < 0:
+            raise ValueError(f"kda_oracle_recurrent failed with code {rc}")
+        self.threads_used = rc
+        return o, fin
+
+    def chunkwise(self, q, k, v, g, beta, scale, chunk_size, initial_state=None,
+                  cu_seqlens=None, num_threads: int = 0):
+        """Chunkwise form in fp64 with any chunk size. Returns (o, final_state)."""
+        q, k, v, g, beta, s0, cu, N, B, T, H, K, V, o, fin = self._prepare(
+            q, k, v, g, beta, initial_state, cu_seqlens)
+        rc = self.lib.kda_oracle_chunkwise(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(s0),
+            _ptr(cu, ctypes.c_int32), N, B, T, H, K, V, int(chunk_size), _ptr(o), _ptr(fin),
+            int(num_threads))
+        if rc < 0:
+            raise ValueError(f"kda_oracle_chunkwise failed with code {rc}")
+        self.threads_used = rc
+        return o, fin
+
+
+_DEFAULT: Optional[Oracle] = None
+
+
+def default_oracle() -> Oracle:
+    """The oracle built from the committed source (built on first use)."""
+    global _DEFAULT
+    if _DEFAULT is None:
+        _DEFAULT = Oracle()
+    return _DEFAULT
