@@ -1,0 +1,148 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) Kimi Delta Attention forward library.
+ *
+ * What is computed (Tokamax "chunk_kda_fwd_design_doc", Appendix 9.1.2, Eq. (1), and
+ * "KDA Doesn't Care About the Future", "Chunkwise KDA in Broad Strokes"): for every
+ * sequence n and head h, a K x V fp32 state S evolves token by token as
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(exp(g_t)) S_{t-1} + beta_t k_t v_t^T,
+ *     o_t = scale * S_t^T q_t,
+ *
+ * starting from initial_state[n,h] (or zero).  The library evaluates it chunk by chunk
+ * (chunk size 64) as in Appendix 9.1.3-9.1.6 (Eq. (6)-(9)): a per-chunk gate cumsum, an
+ * intra-chunk unit-lower-triangular solve giving the W/U representation and the causal
+ * query-key matrix Aqk, the ordered chunk-to-chunk state recurrence and the output.
+ * Packed variable-length sequences (cu_seqlens) never share a chunk or a state
+ * (Appendix 9.1.7).
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor pointers are CUDA device pointers owned by the caller; the library
+ *     keeps no pointer after a call returns and allocates no device memory.
+ *   - Layouts are row-major and token-major:
+ *       q, k : [B, T, H, K]    v, o : [B, T, H, V]    g : [B, T, H, K] (fp32)
+ *       beta : [B, T, H] (fp32)
+ *       initial_state, final_state : [N, H, K, V] (fp32), a state row is a key channel.
+ *     N = B for fixed-length input; N = num_seqs for packed input (then B == 1 and
+ *     sequence n occupies tokens [cu_seqlens[n], cu_seqlens[n+1]) of the T axis).
+ *   - g is the natural-log decay ln(alpha), expected in [-5, 0] (the bound under which
+ *     the 16-key rebasing window of the bf16 path cannot overflow); it is not clamped.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t, NULL = legacy default
+ *     stream), performs no host synchronisation and no allocation.  Arguments are
+ *     validated on the host before anything is enqueued: an error status means that
+ *     nothing was launched and no output was written.
+ *   - Errors are returned, never printed or thrown.
+ *
+ * dtype of q, k, v and o: KDA_DTYPE_BF16 or KDA_DTYPE_F32.  fp32 inputs take an exact
+ * fp32 path (SIMT forward substitution); bf16 inputs with K = V = 128 take the tcgen05
+ * tensor-core path with fp32 accumulation and an fp32 state.
+ */
+#ifndef KDA_H
+#define KDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kda_status {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1,     /* null required pointer, bad size, B != 1 with cu_seqlens */
+    KDA_ERR_UNSUPPORTED = 2,     /* valid but not implemented: chunk_size != 64, K or V not in {64, 128} */
+    KDA_ERR_ALIGNMENT = 3,       /* a pointer is not 16-byte aligned */
+    KDA_ERR_WORKSPACE = 4,       /* workspace null or smaller than kda_fwd_workspace_bytes() */
+    KDA_ERR_CUDA = 5,            /* a CUDA runtime call or kernel launch failed */
+    KDA_ERR_DEVICE_TIMEOUT = 6,  /* a kernel gave up a bounded wait (read via kda_get_device_status) */
+    KDA_ERR_DEVICE = 7           /* no usable sm_103 device is current */
+} kda_status;
+
+typedef enum kda_dtype {
+    KDA_DTYPE_BF16 = 0,
+    KDA_DTYPE_F32 = 1
+} kda_dtype;
+
+/* Bytes of device workspace kda_fwd needs for these sizes (0 on invalid sizes).
+ * Packed input (num_seqs > 0 together with a non-null cu_seqlens at call time) needs
+ * room for ceil(T/64) + num_seqs - 1 chunks per head; fixed length for B * ceil(T/64).
+ * Pass num_seqs = 0 for fixed-length input.  The workspace holds the chunk table, a
+ * device status word and the per-chunk intermediates (W, U, gated keys/queries, Aqk,
+ * chunk decay) that the intra-chunk kernel hands to the recurrence kernel. */
+size_t kda_fwd_workspace_bytes(int B, int T, int H, int K, int V, int num_seqs,
+                               int chunk_size, kda_dtype dtype);
+
+/* Chunkwise KDA forward (Tokamax design doc, 9.1.5-9.1.7, Eq. (6)-(9)).
+ *
+ *   q, k, v        [B,T,H,K], [B,T,H,K], [B,T,H,V] of `dtype`; q and k are used as given
+ *                  (callers L2-normalise them when the model does).
+ *   g, beta        fp32 [B,T,H,K] natural-log decays, fp32 [B,T,H] write strengths.
+ *   scale          output scale (commonly K^-0.5).
+ *   chunk_size     must be 64.
+ *   initial_state  nullable fp32 [N,H,K,V]; NULL means a zero state.
+ *   cu_seqlens     nullable int32 [num_seqs+1] device array, cu_seqlens[0] = 0,
+ *                  non-decreasing, cu_seqlens[num_seqs] = T (a precondition: contents
+ *                  are not read on the host).  Requires B == 1.  Zero-length sequences
+ *                  are allowed and return their initial state.
+ *   num_seqs       number of packed sequences (ignored when cu_seqlens is NULL).
+ *   o              [B,T,H,V] of `dtype`, written for every token.
+ *   final_state    nullable fp32 [N,H,K,V], written when non-NULL.
+ *   B,T,H,K,V      sizes; T need not be a multiple of 64 (the last chunk of a sequence
+ *                  is shorter).  T == 0 (or all sequences empty) writes only final_state.
+ *   workspace      device memory of at least kda_fwd_workspace_bytes(...) bytes,
+ *                  16-byte aligned; contents on entry are ignored.
+ *   stream         cudaStream_t to enqueue on.
+ *
+ * Returns KDA_OK when all launches were enqueued.  Results are deterministic: the
+ * same inputs give bit-identical outputs, and o at token t does not depend on any
+ * input of a later token of the same sequence. */
+kda_status kda_fwd(const void* q, const void* k, const void* v, const float* g,
+                   const float* beta, float scale, int chunk_size,
+                   const float* initial_state, const int32_t* cu_seqlens, int num_seqs,
+                   void* o, float* final_state, int B, int T, int H, int K, int V,
+                   kda_dtype dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/* kda_fwd, plus CUDA events recorded on `stream` around its stages, for timing each
+ * kernel on the stream it runs on.  `events` holds num_events cudaEvent_t handles
+ * created by the caller; events[0] is recorded before the first launch and events[i]
+ * after stage i, for the stages in order: 1 chunk index, 2 intra-chunk kernel,
+ * 3 recurrence/output kernel.  num_events must be 0 (then this is kda_fwd) or at
+ * least 4 (KDA_ERR_INVALID_ARG otherwise).  A stage with nothing to do (T == 0)
+ * still gets its event recorded. */
+kda_status kda_fwd_profiled(const void* q, const void* k, const void* v, const float* g,
+                            const float* beta, float scale, int chunk_size,
+                            const float* initial_state, const int32_t* cu_seqlens,
+                            int num_seqs, void* o, float* final_state, int B, int T, int H,
+                            int K, int V, kda_dtype dtype, void* workspace,
+                            size_t workspace_bytes, void* stream, void* const* events,
+                            int num_events);
+
+/* Build only the chunk index of a (possibly packed) input into `workspace`
+ * (Tokamax design doc 3.5 and 9.1.7: chunks of 64 tokens that never cross a sequence;
+ * the last chunk of a sequence may be shorter).  Writes, at the byte offsets returned
+ * through the optional out-pointers:
+ *   chunk table  int32x4 per chunk c: {sequence n, first token, length, index in sequence}
+ *   seq table    int32x2 per sequence n: {first chunk, number of chunks}
+ *   count        one int32: total number of chunks.
+ * Entries past `count` are left undefined.  Same validation rules as kda_fwd.
+ * kda_fwd performs this step itself; the entry point exists for tests and tools. */
+kda_status kda_build_chunk_index(const int32_t* cu_seqlens, int num_seqs, int B, int T,
+                                 int chunk_size, void* workspace, size_t workspace_bytes,
+                                 size_t* chunk_table_offset, size_t* seq_table_offset,
+                                 size_t* count_offset, void* stream);
+
+/* Human-readable name of a kda_status value (static storage, never NULL). */
+const char* kda_status_string(int status);
+
+/* Reads the device status word that kernels of the last kda_fwd on this workspace
+ * set when they abandon a bounded wait.  Synchronises `stream`.  Returns KDA_OK,
+ * KDA_ERR_DEVICE_TIMEOUT, or KDA_ERR_CUDA if the copy failed. */
+kda_status kda_get_device_status(const void* workspace, void* stream);
+
+/* Version of this ABI (major * 100 + minor). */
+int kda_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H */

@@ -1,0 +1,12 @@
+"""GB300 (sm_103a) Kimi Delta Attention forward: Python binding of libkda_gb300.so.
+
+The compute path is the CUDA library declared in include/kda.h; this package only
+marshals tensors into its C ABI.  Build the library with ``build.build_library()``
+(or ``__graft_entry__.build()``) before use.
+"""
+from ._native import (DTYPE_CODES, KdaError, KdaLibraryMissing, build_chunk_index, fwd,
+                      get_device_status, library_path, load_library, status_string,
+                      workspace_bytes)
+
+__all__ = ["fwd", "workspace_bytes", "build_chunk_index", "get_device_status", "status_string",
+           "load_library", "library_path", "KdaError", "KdaLibraryMissing", "DTYPE_CODES"]

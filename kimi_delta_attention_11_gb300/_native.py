@@ -1,0 +1,189 @@
+"""ctypes binding of libkda_gb300.so (the C ABI in include/kda.h).
+
+Argument marshalling only: tensors are passed as raw device pointers with the current
+CUDA stream; every step of the computation runs in the library's CUDA kernels.  There
+is no fallback: without the built library every call raises ``KdaLibraryMissing``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+KDA_OK = 0
+STATUS_NAMES = {
+    0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED", 3: "KDA_ERR_ALIGNMENT",
+    4: "KDA_ERR_WORKSPACE", 5: "KDA_ERR_CUDA", 6: "KDA_ERR_DEVICE_TIMEOUT", 7: "KDA_ERR_DEVICE",
+}
+DTYPE_CODES = {torch.bfloat16: 0, torch.float32: 1}
+
+
+class KdaLibraryMissing(RuntimeError):
+    """The CUDA library has not been built (run __graft_entry__.build())."""
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)} "
+                         f"({status_string(status)})")
+
+
+_LIB = None
+_LOCK = threading.Lock()
+
+_vp, _sz, _i, _f = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_float
+_SIGNATURES = {
+    "kda_fwd_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i, _i, _i]),
+    "kda_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _f, _i, _vp, _vp, _i, _vp, _vp,
+                     _i, _i, _i, _i, _i, _i, _vp, _sz, _vp]),
+    "kda_fwd_profiled": (_i, [_vp, _vp, _vp, _vp, _vp, _f, _i, _vp, _vp, _i, _vp, _vp,
+                              _i, _i, _i, _i, _i, _i, _vp, _sz, _vp,
+                              ctypes.POINTER(ctypes.c_void_p), _i]),
+    "kda_build_chunk_index": (_i, [_vp, _i, _i, _i, _i, _vp, _sz, ctypes.POINTER(_sz),
+                                   ctypes.POINTER(_sz), ctypes.POINTER(_sz), _vp]),
+    "kda_status_string": (ctypes.c_char_p, [_i]),
+    "kda_get_device_status": (_i, [_vp, _vp]),
+    "kda_abi_version": (_i, []),
+}
+
+
+def library_path() -> str:
+    return _build.LIBRARY
+
+
+def load_library(path: Optional[str] = None):
+    """Load (once) and return the ctypes handle of libkda_gb300.so."""
+    global _LIB
+    with _LOCK:
+        if _LIB is not None and path is None:
+            return _LIB
+        p = path or library_path()
+        if not os.path.exists(p):
+            raise KdaLibraryMissing(
+                f"{p} not found: build the CUDA library first (__graft_entry__.build())")
+        lib = ctypes.CDLL(p)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        if path is None:
+            _LIB = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return load_library().kda_status_string(int(status)).decode()
+    except KdaLibraryMissing:
+        return STATUS_NAMES.get(status, "unknown")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(device: torch.device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def workspace_bytes(B: int, T: int, H: int, K: int, V: int, num_seqs: int = 0,
+                    dtype: torch.dtype = torch.bfloat16, chunk_size: int = 64) -> int:
+    n = load_library().kda_fwd_workspace_bytes(B, T, H, K, V, num_seqs, chunk_size,
+                                               DTYPE_CODES[dtype])
+    if n == 0:
+        raise KdaError(1, "kda_fwd_workspace_bytes")
+    return int(n)
+
+
+def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+        beta: torch.Tensor, scale: Optional[float] = None,
+        initial_state: Optional[torch.Tensor] = None,
+        cu_seqlens: Optional[torch.Tensor] = None, output_final_state: bool = True,
+        chunk_size: int = 64, workspace: Optional[torch.Tensor] = None,
+        out: Optional[torch.Tensor] = None, final_state: Optional[torch.Tensor] = None,
+        events=None):
+    """Chunkwise KDA forward on the current CUDA stream (no host synchronisation).
+
+    q, k: [B,T,H,K]; v: [B,T,H,V] (bf16 or fp32, all the same dtype); g: [B,T,H,K] fp32;
+    beta: [B,T,H] fp32; initial_state: optional [N,H,K,V] fp32; cu_seqlens: optional
+    int32 [N+1] (then B == 1).  Returns (o [B,T,H,V] in q.dtype, final_state [N,H,K,V]
+    fp32 or None).  ``workspace``/``out``/``final_state`` may be passed to reuse memory.
+    ``events``: optional list of >= 4 ``torch.cuda.Event`` recorded around the stages
+    (chunk index, intra-chunk kernel, recurrence kernel) for per-kernel timing.
+    """
+    lib = load_library()
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    if scale is None:
+        scale = K ** -0.5
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if k.dtype != q.dtype or v.dtype != q.dtype or q.dtype not in DTYPE_CODES:
+        raise ValueError("q, k, v must share one dtype, bf16 or fp32")
+    if g.dtype != torch.float32 or beta.dtype != torch.float32:
+        raise ValueError("g and beta must be fp32")
+    if initial_state is not None and (initial_state.dtype != torch.float32
+                                      or not initial_state.is_contiguous()):
+        raise ValueError("initial_state must be contiguous fp32")
+    num_seqs = 0
+    if cu_seqlens is not None:
+        if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda:
+            raise ValueError("cu_seqlens must be an int32 CUDA tensor")
+        num_seqs = cu_seqlens.numel() - 1
+    N = num_seqs if cu_seqlens is not None else B
+    dev = q.device
+    need = workspace_bytes(B, T, H, K, V, num_seqs, q.dtype, chunk_size)
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    o = out if out is not None else torch.empty((B, T, H, V), dtype=q.dtype, device=dev)
+    fin = final_state
+    if fin is None and output_final_state:
+        fin = torch.empty((N, H, K, V), dtype=torch.float32, device=dev)
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), chunk_size,
+            _ptr(initial_state), _ptr(cu_seqlens), num_seqs, _ptr(o), _ptr(fin),
+            B, T, H, K, V, DTYPE_CODES[q.dtype], _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _stream_handle(dev))
+    if events is None:
+        st = lib.kda_fwd(*args)
+    else:
+        handles = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+        st = lib.kda_fwd_profiled(*args, handles, len(events))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_fwd")
+    return o, fin
+
+
+def build_chunk_index(cu_seqlens: Optional[torch.Tensor], B: int, T: int,
+                      device: Optional[torch.device] = None, chunk_size: int = 64):
+    """Run the chunk-index kernel alone. Returns (chunk_table [n,4], seq_table [N,2],
+    count) as int32 tensors read back to the host (this synchronises)."""
+    lib = load_library()
+    num_seqs = cu_seqlens.numel() - 1 if cu_seqlens is not None else 0
+    dev = device or (cu_seqlens.device if cu_seqlens is not None else torch.device("cuda"))
+    need = workspace_bytes(B, T, 1, 64, 64, num_seqs, torch.float32, chunk_size)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    offs = [ctypes.c_size_t(0) for _ in range(3)]
+    st = lib.kda_build_chunk_index(_ptr(cu_seqlens), num_seqs, B, T, chunk_size, _ptr(ws), need,
+                                   ctypes.byref(offs[0]), ctypes.byref(offs[1]),
+                                   ctypes.byref(offs[2]), _stream_handle(dev))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_build_chunk_index")
+    wsh = ws.cpu()
+    count = int(wsh[offs[2].value:offs[2].value + 4].view(torch.int32)[0])
+    N = num_seqs if cu_seqlens is not None else B
+    ctab = wsh[offs[0].value:offs[0].value + 16 * count].view(torch.int32).view(count, 4)
+    stab = wsh[offs[1].value:offs[1].value + 8 * N].view(torch.int32).view(N, 2)
+    return ctab.clone(), stab.clone(), count
+
+
+def get_device_status(workspace: torch.Tensor) -> int:
+    """Status word the kernels of the last kda_fwd on `workspace` left (synchronises)."""
+    return int(load_library().kda_get_device_status(_ptr(workspace),
+                                                    _stream_handle(workspace.device)))

@@ -1,0 +1,183 @@
+// kda_api.cu -- the C ABI entry points declared in include/kda.h.
+//
+// Host-side validation happens before anything is enqueued; then the chunk index, the
+// intra-chunk stage and the state/output recurrence are launched on the caller's
+// stream with no host synchronisation and no allocation.
+#include <limits.h>
+
+#include "kda_internal.cuh"
+
+namespace kda {
+
+Layout make_layout(int B, int T, int H, int K, int V, int num_seqs, bool packed, kda_dtype dt) {
+    Layout L;
+    const long long nct = ((long long)T + kChunk - 1) / kChunk;
+    L.N = packed ? num_seqs : B;
+    if (packed)
+        L.max_chunks = T > 0 ? nct + num_seqs - 1 : 0;
+    else
+        L.max_chunks = (long long)B * nct;
+    L.chunk_tab_off = 256;
+    L.seq_tab_off = align_up(L.chunk_tab_off + (size_t)L.max_chunks * 16, 256);
+    L.inter_off = align_up(L.seq_tab_off + (size_t)L.N * 8, 1024);
+    (void)dt;
+    L.inter_stride = align_up(SimtRecord::floats(K, V) * sizeof(float), 1024);
+    L.total = L.inter_off + (size_t)L.max_chunks * H * L.inter_stride;
+    return L;
+}
+
+}  // namespace kda
+
+using namespace kda;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Size and shape rules shared by kda_fwd and kda_fwd_workspace_bytes.
+kda_status check_sizes(int B, int T, int H, int K, int V, int num_seqs, bool packed,
+                       int chunk_size, kda_dtype dt) {
+    if (B < 1 || T < 0 || H < 1 || K < 1 || V < 1) return KDA_ERR_INVALID_ARG;
+    if (dt != KDA_DTYPE_BF16 && dt != KDA_DTYPE_F32) return KDA_ERR_INVALID_ARG;
+    // State propagation is defined for K <= 256 (Tokamax design doc, 5.3).
+    if (K > 256 || V > 256) return KDA_ERR_INVALID_ARG;
+    if (packed && (B != 1 || num_seqs < 1)) return KDA_ERR_INVALID_ARG;
+    // every element index must fit the kernels' 64-bit arithmetic and every token
+    // index a 32-bit int
+    if ((long long)B * T >= INT_MAX) return KDA_ERR_INVALID_ARG;
+    if (chunk_size != kChunk) return KDA_ERR_UNSUPPORTED;
+    if ((K != 64 && K != 128) || (V != 64 && V != 128)) return KDA_ERR_UNSUPPORTED;
+    return KDA_OK;
+}
+
+// The library is built for sm_103a only; refuse any other current device up front.
+kda_status check_device() {
+    static int verdict[64];  // 0 unknown, 1 ok, 2 unusable
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return KDA_ERR_DEVICE;
+    }
+    if (verdict[dev] == 0) {
+        int major = 0, minor = 0;
+        const bool ok = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) ==
+                            cudaSuccess &&
+                        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) ==
+                            cudaSuccess &&
+                        major == 10 && minor == 3;
+        cudaGetLastError();
+        verdict[dev] = ok ? 1 : 2;
+    }
+    return verdict[dev] == 1 ? KDA_OK : KDA_ERR_DEVICE;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kda_abi_version(void) { return 100; }
+
+const char* kda_status_string(int status) {
+    switch (status) {
+        case KDA_OK: return "ok";
+        case KDA_ERR_INVALID_ARG: return "invalid argument";
+        case KDA_ERR_UNSUPPORTED: return "unsupported configuration";
+        case KDA_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+        case KDA_ERR_WORKSPACE: return "workspace missing or too small";
+        case KDA_ERR_CUDA: return "CUDA runtime error";
+        case KDA_ERR_DEVICE_TIMEOUT: return "device-side bounded wait expired";
+        case KDA_ERR_DEVICE: return "no usable sm_103 device";
+        default: return "unknown status";
+    }
+}
+
+size_t kda_fwd_workspace_bytes(int B, int T, int H, int K, int V, int num_seqs, int chunk_size,
+                               kda_dtype dtype) {
+    const bool packed = num_seqs > 0;
+    if (check_sizes(B, T, H, K, V, num_seqs, packed, chunk_size, dtype) != KDA_OK) return 0;
+    return make_layout(B, T, H, K, V, num_seqs, packed, dtype).total;
+}
+
+kda_status kda_build_chunk_index(const int32_t* cu_seqlens, int num_seqs, int B, int T,
+                                 int chunk_size, void* workspace, size_t workspace_bytes,
+                                 size_t* chunk_table_offset, size_t* seq_table_offset,
+                                 size_t* count_offset, void* stream) {
+    const bool packed = cu_seqlens != nullptr;
+    if (B < 1 || T < 0 || (packed && (B != 1 || num_seqs < 1))) return KDA_ERR_INVALID_ARG;
+    if ((long long)B * T >= INT_MAX) return KDA_ERR_INVALID_ARG;
+    if (chunk_size != kChunk) return KDA_ERR_UNSUPPORTED;
+    if (!workspace) return KDA_ERR_WORKSPACE;
+    if (!aligned16(workspace) || (packed && (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)))
+        return KDA_ERR_ALIGNMENT;
+    const Layout L = make_layout(B, T, 1, 64, 64, num_seqs, packed, KDA_DTYPE_F32);
+    const size_t need = L.inter_off;  // index part only
+    if (workspace_bytes < need) return KDA_ERR_WORKSPACE;
+    if (chunk_table_offset) *chunk_table_offset = L.chunk_tab_off;
+    if (seq_table_offset) *seq_table_offset = L.seq_tab_off;
+    if (count_offset) *count_offset = L.count_off;
+    if (kda_status d = check_device()) return d;
+    char* ws = static_cast<char*>(workspace);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(ws, 0, 256, s) != cudaSuccess) return KDA_ERR_CUDA;
+    if (launch_chunk_index(cu_seqlens, L.N, T, L, ws, s) != cudaSuccess) return KDA_ERR_CUDA;
+    return KDA_OK;
+}
+
+kda_status kda_fwd_profiled(const void* q, const void* k, const void* v, const float* g,
+                            const float* beta, float scale, int chunk_size,
+                            const float* initial_state, const int32_t* cu_seqlens, int num_seqs,
+                            void* o, float* final_state, int B, int T, int H, int K, int V,
+                            kda_dtype dtype, void* workspace, size_t workspace_bytes,
+                            void* stream, void* const* events, int num_events) {
+    const bool packed = cu_seqlens != nullptr;
+    if (kda_status st = check_sizes(B, T, H, K, V, num_seqs, packed, chunk_size, dtype))
+        return st;
+    if (!q || !k || !v || !g || !beta || !o) return KDA_ERR_INVALID_ARG;
+    if (num_events != 0 && (num_events < 4 || !events)) return KDA_ERR_INVALID_ARG;
+    if (!workspace) return KDA_ERR_WORKSPACE;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(beta) ||
+        !aligned16(o) || !aligned16(workspace) || (initial_state && !aligned16(initial_state)) ||
+        (final_state && !aligned16(final_state)) ||
+        (packed && (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)))
+        return KDA_ERR_ALIGNMENT;
+    const Layout L = make_layout(B, T, H, K, V, num_seqs, packed, dtype);
+    if (workspace_bytes < L.total) return KDA_ERR_WORKSPACE;
+    if (kda_status d = check_device()) return d;
+
+    char* ws = static_cast<char*>(workspace);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    auto mark = [&](int i) {
+        return num_events == 0 ||
+               cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) == cudaSuccess;
+    };
+    if (!mark(0)) return KDA_ERR_CUDA;
+    if (cudaMemsetAsync(ws, 0, 256, s) != cudaSuccess) return KDA_ERR_CUDA;
+    if (launch_chunk_index(cu_seqlens, L.N, T, L, ws, s) != cudaSuccess) return KDA_ERR_CUDA;
+    if (!mark(1)) return KDA_ERR_CUDA;
+    if (launch_simt(q, k, v, g, beta, scale, initial_state, o, final_state, H, K, V, dtype, L, ws,
+                    s, num_events ? events + 2 : nullptr) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    return KDA_OK;
+}
+
+kda_status kda_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                   float scale, int chunk_size, const float* initial_state,
+                   const int32_t* cu_seqlens, int num_seqs, void* o, float* final_state, int B,
+                   int T, int H, int K, int V, kda_dtype dtype, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+    return kda_fwd_profiled(q, k, v, g, beta, scale, chunk_size, initial_state, cu_seqlens,
+                            num_seqs, o, final_state, B, T, H, K, V, dtype, workspace,
+                            workspace_bytes, stream, nullptr, 0);
+}
+
+kda_status kda_get_device_status(const void* workspace, void* stream) {
+    if (!workspace) return KDA_ERR_WORKSPACE;
+    int word = 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    return word == 0 ? KDA_OK : static_cast<kda_status>(word);
+}
+
+}  // extern "C"

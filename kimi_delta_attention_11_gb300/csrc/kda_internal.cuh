@@ -1,0 +1,62 @@
+// kda_internal.cuh -- shared definitions of the CUDA library (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/kda.h"
+
+namespace kda {
+
+constexpr int kChunk = 64;  // chunk size C: the production path fixes C = 64
+
+// Byte layout of the caller's workspace.
+//   [0, 4)       int32 device status word (0 = ok, else a kda_status)
+//   [16, 20)     int32 number of chunks, written by the chunk-index kernel
+//   chunk table  int4 per chunk   {sequence, first token, length, index in sequence}
+//   seq table    int2 per sequence {first chunk, number of chunks}
+//   inter        per (chunk, head) intermediates of the intra-chunk stage
+struct Layout {
+    size_t status_off = 0;
+    size_t count_off = 16;
+    size_t chunk_tab_off = 0;
+    size_t seq_tab_off = 0;
+    size_t inter_off = 0;
+    size_t inter_stride = 0;  // bytes per (chunk, head)
+    size_t total = 0;
+    long long max_chunks = 0;
+    int N = 0;
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Per-(chunk, head) intermediate record of the fp32 path (all fp32, row-major):
+//   W [C][K], U [C][V], Kbar [C][K], Qg [C][K], Aqk [C][C], gamma [K]
+struct SimtRecord {
+    __host__ __device__ static size_t w(int) { return 0; }
+    __host__ __device__ static size_t u(int K) { return (size_t)kChunk * K; }
+    __host__ __device__ static size_t kbar(int K, int V) { return u(K) + (size_t)kChunk * V; }
+    __host__ __device__ static size_t qg(int K, int V) { return kbar(K, V) + (size_t)kChunk * K; }
+    __host__ __device__ static size_t aqk(int K, int V) { return qg(K, V) + (size_t)kChunk * K; }
+    __host__ __device__ static size_t gamma(int K, int V) { return aqk(K, V) + (size_t)kChunk * kChunk; }
+    __host__ __device__ static size_t floats(int K, int V) { return gamma(K, V) + K; }
+};
+
+Layout make_layout(int B, int T, int H, int K, int V, int num_seqs, bool packed, kda_dtype dt);
+
+// Launchers (return cudaGetLastError() of their launches).
+cudaError_t launch_chunk_index(const int32_t* cu_seqlens, int N, int T, const Layout& L,
+                               char* ws, cudaStream_t s);
+cudaError_t launch_simt(const void* q, const void* k, const void* v, const float* g,
+                        const float* beta, float scale, const float* s0, void* o, float* sN,
+                        int H, int K, int V, kda_dtype dt, const Layout& L, char* ws,
+                        cudaStream_t s, void* const* events_after);
+
+// Records events_after[i] (a cudaEvent_t) on s when events_after is non-null.
+inline bool record_event(void* const* events_after, int i, cudaStream_t s) {
+    return !events_after ||
+           cudaEventRecord(static_cast<cudaEvent_t>(events_after[i]), s) == cudaSuccess;
+}
+
+}  // namespace kda

@@ -1,0 +1,111 @@
+"""C-ABI contract checks that need no GPU: the library loads, exports every function
+that include/kda.h declares, and rejects invalid arguments before launching anything."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import kimi_delta_attention_11_gb300 as kda
+from kimi_delta_attention_11_gb300 import _native
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "kda.h")
+
+OK, INVALID, UNSUPPORTED, ALIGN, WORKSPACE, CUDA, TIMEOUT, DEVICE = range(8)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z_0-9]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return kda.load_library()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert "kda_fwd" in names and len(names) >= 6
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in kda.h but not exported"
+        assert n in _native._SIGNATURES, f"{n} has no binding signature"
+
+
+def test_status_strings(lib):
+    for s in range(8):
+        assert lib.kda_status_string(s).decode()
+    assert lib.kda_status_string(99).decode() == "unknown status"
+    assert lib.kda_abi_version() == 100
+
+
+def test_workspace_bytes_rules(lib):
+    ws = lambda *a: lib.kda_fwd_workspace_bytes(*a)
+    bf16, f32 = 0, 1
+    assert ws(2, 4096, 16, 128, 128, 0, 64, bf16) > 0
+    assert ws(2, 4096, 16, 128, 128, 0, 32, bf16) == 0        # chunk size
+    assert ws(2, 4096, 16, 96, 128, 0, 64, bf16) == 0         # K unsupported
+    assert ws(2, 4096, 16, 512, 128, 0, 64, bf16) == 0        # K > 256
+    assert ws(0, 4096, 16, 128, 128, 0, 64, bf16) == 0        # B
+    assert ws(1, 5000, 4, 64, 64, 3, 64, f32) >= ws(1, 5000, 4, 64, 64, 1, 64, f32)
+    assert ws(2, 0, 1, 64, 64, 0, 64, f32) > 0                # T = 0 is valid
+    assert ws(1, 1000, 8, 128, 128, 2, 64, bf16) >= ws(1, 1000, 8, 128, 128, 1, 64, bf16)
+
+
+FAKE = 0x10000  # an aligned address that is never dereferenced: calls fail validation
+
+
+def call_fwd(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, scale=0.1, chunk=64, s0=None, cu=None,
+             nseq=0, o=FAKE, fin=None, B=1, T=64, H=1, K=64, V=64, dt=1, ws=FAKE,
+             wsb=1 << 40, stream=None)
+    a.update(kw)
+    return lib.kda_fwd(a["q"], a["k"], a["v"], a["g"], a["beta"], a["scale"], a["chunk"], a["s0"],
+                       a["cu"], a["nseq"], a["o"], a["fin"], a["B"], a["T"], a["H"], a["K"],
+                       a["V"], a["dt"], a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), INVALID), (dict(beta=None), INVALID), (dict(o=None), INVALID),
+    (dict(B=0), INVALID), (dict(T=-1), INVALID), (dict(H=0), INVALID),
+    (dict(K=512), INVALID), (dict(V=300), INVALID), (dict(dt=7), INVALID),
+    (dict(cu=FAKE, nseq=2, B=2), INVALID), (dict(cu=FAKE, nseq=0), INVALID),
+    (dict(chunk=32), UNSUPPORTED), (dict(K=96), UNSUPPORTED), (dict(V=32), UNSUPPORTED),
+    (dict(q=FAKE + 8), ALIGN), (dict(o=FAKE + 4), ALIGN), (dict(s0=FAKE + 2), ALIGN),
+    (dict(fin=FAKE + 12), ALIGN), (dict(cu=FAKE + 2, nseq=1), ALIGN), (dict(ws=FAKE + 8), ALIGN),
+    (dict(ws=None), WORKSPACE), (dict(wsb=16), WORKSPACE),
+])
+def test_fwd_rejects_before_launch(lib, kw, status):
+    assert call_fwd(lib, **kw) == status
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="only meaningful without a GPU")
+def test_valid_call_without_gpu_reports_device(lib):
+    assert call_fwd(lib) == DEVICE
+
+
+def test_profiled_rejects_short_event_list(lib):
+    a = [FAKE, FAKE, FAKE, FAKE, FAKE, 0.1, 64, None, None, 0, FAKE, None, 1, 64, 1, 64, 64, 1,
+         FAKE, 1 << 40, None]
+    evs = (ctypes.c_void_p * 2)()
+    assert lib.kda_fwd_profiled(*a, evs, 2) == INVALID
+    assert lib.kda_fwd_profiled(*a, None, 4) == INVALID
+    a[0] = None
+    assert lib.kda_fwd_profiled(*a, None, 0) == INVALID
+
+
+def test_chunk_index_rejects(lib):
+    off = ctypes.c_size_t(0)
+    f = lib.kda_build_chunk_index
+    assert f(None, 0, 0, 10, 64, FAKE, 1 << 30, None, None, None, None) == INVALID
+    assert f(FAKE, 2, 2, 10, 64, FAKE, 1 << 30, None, None, None, None) == INVALID
+    assert f(None, 0, 1, 10, 32, FAKE, 1 << 30, None, None, None, None) == UNSUPPORTED
+    assert f(None, 0, 1, 10, 64, None, 1 << 30, None, None, None, None) == WORKSPACE
+    assert f(None, 0, 1, 10, 64, FAKE, 8, ctypes.byref(off), None, None, None) == WORKSPACE
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    with pytest.raises(kda.KdaLibraryMissing):
+        _native.load_library(str(tmp_path / "missing.so"))
