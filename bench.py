@@ -294,6 +294,8 @@ def run_ours(args, rank, world, local):
 
     # timed region: K steps, per-stage CUDA events on the launching stream
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    for e in (x for row in evs for x in row):   # torch creates the CUDA event on first record
+        e.record(stream)
     barrier(world)
     torch.cuda.synchronize()
     wall0 = time.perf_counter()

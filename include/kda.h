@@ -50,7 +50,7 @@ typedef enum kda_status {
     KDA_OK = 0,
     KDA_ERR_INVALID_ARG = 1,     /* null required pointer, bad size, B != 1 with cu_seqlens */
     KDA_ERR_UNSUPPORTED = 2,     /* valid but not implemented: chunk_size != 64, K or V not in {64, 128} */
-    KDA_ERR_ALIGNMENT = 3,       /* a pointer is not 16-byte aligned */
+    KDA_ERR_ALIGNMENT = 3,       /* a pointer is misaligned (16 bytes; 4 for beta and cu_seqlens) */
     KDA_ERR_WORKSPACE = 4,       /* workspace null or smaller than kda_fwd_workspace_bytes() */
     KDA_ERR_CUDA = 5,            /* a CUDA runtime call or kernel launch failed */
     KDA_ERR_DEVICE_TIMEOUT = 6,  /* a kernel gave up a bounded wait (read via kda_get_device_status) */
@@ -87,7 +87,10 @@ size_t kda_fwd_workspace_bytes(int B, int T, int H, int K, int V, int num_seqs,
  *   o              [B,T,H,V] of `dtype`, written for every token.
  *   final_state    nullable fp32 [N,H,K,V], written when non-NULL.
  *   B,T,H,K,V      sizes; T need not be a multiple of 64 (the last chunk of a sequence
- *                  is shorter).  T == 0 (or all sequences empty) writes only final_state.
+ *                  is shorter).  T == 0 (or all sequences empty) writes only final_state;
+ *                  with T == 0 the token tensors are not accessed and may be NULL.
+ *   alignment      q, k, v, g, o, the states and the workspace 16 bytes; beta and
+ *                  cu_seqlens 4 bytes (so a token slice of any tensor stays valid).
  *   workspace      device memory of at least kda_fwd_workspace_bytes(...) bytes,
  *                  16-byte aligned; contents on entry are ignored.
  *   stream         cudaStream_t to enqueue on.

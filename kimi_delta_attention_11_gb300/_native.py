@@ -153,6 +153,8 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
     if events is None:
         st = lib.kda_fwd(*args)
     else:
+        if any(e.cuda_event == 0 for e in events):
+            raise ValueError("events must have been created (record each once before use)")
         handles = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
         st = lib.kda_fwd_profiled(*args, handles, len(events))
     if st != KDA_OK:

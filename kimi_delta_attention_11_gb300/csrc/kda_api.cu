@@ -33,6 +33,7 @@ using namespace kda;
 namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 // Size and shape rules shared by kda_fwd and kda_fwd_workspace_bytes.
 kda_status check_sizes(int B, int T, int H, int K, int V, int num_seqs, bool packed,
@@ -107,8 +108,7 @@ kda_status kda_build_chunk_index(const int32_t* cu_seqlens, int num_seqs, int B,
     if ((long long)B * T >= INT_MAX) return KDA_ERR_INVALID_ARG;
     if (chunk_size != kChunk) return KDA_ERR_UNSUPPORTED;
     if (!workspace) return KDA_ERR_WORKSPACE;
-    if (!aligned16(workspace) || (packed && (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)))
-        return KDA_ERR_ALIGNMENT;
+    if (!aligned16(workspace) || (packed && !aligned4(cu_seqlens))) return KDA_ERR_ALIGNMENT;
     const Layout L = make_layout(B, T, 1, 64, 64, num_seqs, packed, KDA_DTYPE_F32);
     const size_t need = L.inter_off;  // index part only
     if (workspace_bytes < need) return KDA_ERR_WORKSPACE;
@@ -132,13 +132,15 @@ kda_status kda_fwd_profiled(const void* q, const void* k, const void* v, const f
     const bool packed = cu_seqlens != nullptr;
     if (kda_status st = check_sizes(B, T, H, K, V, num_seqs, packed, chunk_size, dtype))
         return st;
-    if (!q || !k || !v || !g || !beta || !o) return KDA_ERR_INVALID_ARG;
+    // With T == 0 no token tensor is read or written, so its pointers may be anything.
+    const bool tokens = T > 0;
+    if (tokens && (!q || !k || !v || !g || !beta || !o)) return KDA_ERR_INVALID_ARG;
     if (num_events != 0 && (num_events < 4 || !events)) return KDA_ERR_INVALID_ARG;
     if (!workspace) return KDA_ERR_WORKSPACE;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(beta) ||
-        !aligned16(o) || !aligned16(workspace) || (initial_state && !aligned16(initial_state)) ||
-        (final_state && !aligned16(final_state)) ||
-        (packed && (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)))
+    if ((tokens && (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) ||
+                    !aligned4(beta) || !aligned16(o))) ||
+        !aligned16(workspace) || (initial_state && !aligned16(initial_state)) ||
+        (final_state && !aligned16(final_state)) || (packed && !aligned4(cu_seqlens)))
         return KDA_ERR_ALIGNMENT;
     const Layout L = make_layout(B, T, H, K, V, num_seqs, packed, dtype);
     if (workspace_bytes < L.total) return KDA_ERR_WORKSPACE;

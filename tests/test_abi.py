@@ -74,6 +74,7 @@ def call_fwd(lib, **kw):
     (dict(cu=FAKE, nseq=2, B=2), INVALID), (dict(cu=FAKE, nseq=0), INVALID),
     (dict(chunk=32), UNSUPPORTED), (dict(K=96), UNSUPPORTED), (dict(V=32), UNSUPPORTED),
     (dict(q=FAKE + 8), ALIGN), (dict(o=FAKE + 4), ALIGN), (dict(s0=FAKE + 2), ALIGN),
+    (dict(beta=FAKE + 2), ALIGN), (dict(g=FAKE + 4), ALIGN),
     (dict(fin=FAKE + 12), ALIGN), (dict(cu=FAKE + 2, nseq=1), ALIGN), (dict(ws=FAKE + 8), ALIGN),
     (dict(ws=None), WORKSPACE), (dict(wsb=16), WORKSPACE),
 ])
@@ -84,6 +85,8 @@ def test_fwd_rejects_before_launch(lib, kw, status):
 @pytest.mark.skipif(torch.cuda.is_available(), reason="only meaningful without a GPU")
 def test_valid_call_without_gpu_reports_device(lib):
     assert call_fwd(lib) == DEVICE
+    assert call_fwd(lib, beta=FAKE + 4) == DEVICE          # beta needs 4-byte alignment only
+    assert call_fwd(lib, q=None, k=None, v=None, g=None, beta=None, o=None, T=0) == DEVICE
 
 
 def test_profiled_rejects_short_event_list(lib):
