@@ -133,6 +133,34 @@ kda_status kda_build_chunk_index(const int32_t* cu_seqlens, int num_seqs, int B,
                                  size_t* chunk_table_offset, size_t* seq_table_offset,
                                  size_t* count_offset, void* stream);
 
+/* Size of the scratch area compiled into the library for kda_fwd_noalloc (64 MiB). */
+#define KDA_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+/* kda_fwd without a caller-provided workspace.  (The KDA pages have no counterpart to
+ * this entry point; it exists for callers of this library that cannot allocate.)
+ *
+ * Who needs it: callers that cannot obtain device memory for the workspace, e.g. a
+ * plug-in whose host application owns every device allocation, a request path on which
+ * allocating is forbidden because cudaMalloc/cudaFree may synchronise the device, or a
+ * binding without any device allocator.  The call allocates nothing: its workspace is a
+ * fixed device array of KDA_NOALLOC_SCRATCH_BYTES bytes inside the library.
+ *
+ * Arguments, layouts and results are those of kda_fwd (minus workspace and its size).
+ * Rules specific to this entry point:
+ *   - problems with kda_fwd_workspace_bytes(...) > KDA_NOALLOC_SCRATCH_BYTES are
+ *     rejected with KDA_ERR_WORKSPACE before anything is launched;
+ *   - every GPU on which the library's module is loaded keeps the array until exit;
+ *   - all calls on a device share the array and it keeps the previous call's contents
+ *     (the call resets what must start at zero); calls whose GPU work overlaps (e.g. on
+ *     two unordered streams) race on it and must be serialised by the caller;
+ *   - the first call on each device looks up the array's address with that device
+ *     current; make it before any stream capture. */
+kda_status kda_fwd_noalloc(const void* q, const void* k, const void* v, const float* g,
+                           const float* beta, float scale, int chunk_size,
+                           const float* initial_state, const int32_t* cu_seqlens,
+                           int num_seqs, void* o, float* final_state, int B, int T, int H,
+                           int K, int V, kda_dtype dtype, void* stream);
+
 /* Human-readable name of a kda_status value (static storage, never NULL). */
 const char* kda_status_string(int status);
 

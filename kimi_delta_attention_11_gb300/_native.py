@@ -45,6 +45,8 @@ _SIGNATURES = {
     "kda_fwd_profiled": (_i, [_vp, _vp, _vp, _vp, _vp, _f, _i, _vp, _vp, _i, _vp, _vp,
                               _i, _i, _i, _i, _i, _i, _vp, _sz, _vp,
                               ctypes.POINTER(ctypes.c_void_p), _i]),
+    "kda_fwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _f, _i, _vp, _vp, _i, _vp, _vp,
+                             _i, _i, _i, _i, _i, _i, _vp]),
     "kda_build_chunk_index": (_i, [_vp, _i, _i, _i, _i, _vp, _sz, ctypes.POINTER(_sz),
                                    ctypes.POINTER(_sz), ctypes.POINTER(_sz), _vp]),
     "kda_status_string": (ctypes.c_char_p, [_i]),
