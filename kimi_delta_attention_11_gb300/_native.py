@@ -49,6 +49,7 @@ _SIGNATURES = {
                              _i, _i, _i, _i, _i, _i, _vp]),
     "kda_build_chunk_index": (_i, [_vp, _i, _i, _i, _i, _vp, _sz, ctypes.POINTER(_sz),
                                    ctypes.POINTER(_sz), ctypes.POINTER(_sz), _vp]),
+    "kda_selftest_umma": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp, _vp]),
     "kda_status_string": (ctypes.c_char_p, [_i]),
     "kda_get_device_status": (_i, [_vp, _vp]),
     "kda_abi_version": (_i, []),
@@ -185,6 +186,22 @@ def build_chunk_index(cu_seqlens: Optional[torch.Tensor], B: int, T: int,
     ctab = wsh[offs[0].value:offs[0].value + 16 * count].view(torch.int32).view(count, 4)
     stab = wsh[offs[1].value:offs[1].value + 8 * N].view(torch.int32).view(N, 2)
     return ctab.clone(), stab.clone(), count
+
+
+def selftest_umma(A: torch.Tensor, B: torch.Tensor, mode: int = 0) -> torch.Tensor:
+    """Diagnostic tcgen05 GEMM: returns A[128,K] @ B[N,K]^T in fp32 (synchronises)."""
+    lib = load_library()
+    N, K = B.shape
+    D = torch.empty((A.shape[0], N), dtype=torch.float32, device=A.device)
+    status = torch.zeros(1, dtype=torch.int32, device=A.device)
+    st = lib.kda_selftest_umma(_ptr(A), _ptr(B), _ptr(D), N, K, mode, _ptr(status),
+                               _stream_handle(A.device))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_selftest_umma")
+    torch.cuda.synchronize(A.device)
+    if int(status.item()) != 0:
+        raise KdaError(int(status.item()), "kda_selftest_umma (device)")
+    return D
 
 
 def get_device_status(workspace: torch.Tensor) -> int:

@@ -1,6 +1,7 @@
 // kda_internal.cuh -- shared definitions of the CUDA library (not part of the ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -42,6 +43,12 @@ struct SimtRecord {
     __host__ __device__ static size_t gamma(int K, int V) { return aqk(K, V) + (size_t)kChunk * kChunk; }
     __host__ __device__ static size_t floats(int K, int V) { return gamma(K, V) + K; }
 };
+
+// 2-D TMA tensor map over a row-major matrix of `outer` rows x `inner` elements
+// (bf16 or fp32), box of box_outer rows x box_inner elements, optional 128-byte swizzle,
+// zero fill outside the tensor.  Returns false if the driver rejects it.
+bool make_tmap_2d(CUtensorMap* map, const void* base, bool bf16, uint64_t inner, uint64_t outer,
+                  uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, bool swizzle128);
 
 Layout make_layout(int B, int T, int H, int K, int V, int num_seqs, bool packed, kda_dtype dt);
 
