@@ -354,11 +354,13 @@ def run_ours(args, rank, world, local):
         return 0
     tokens_all = alg["tokens"] * world
     value = tokens_all / (ms * 1e-3)
-    names = ["kda_chunk_index", "kda_intra", "kda_h_o"]
+    tc = inp["dtype"] == torch.bfloat16 and K == 128 and V == 128
+    names = (["kda_chunk_index", "kda_intra_tc", "kda_h_o_tc"] if tc
+             else ["kda_chunk_index", "kda_intra_simt", "kda_h_o_simt"])
     avg = [sum(s[j] for s in stage_ms) / args.steps for j in range(3)]
     dom = max(range(3), key=lambda j: avg[j])
-    kb = {"kda_chunk_index": 0, "kda_intra": alg["in_bytes"],
-          "kda_h_o": alg["out_bytes"] + alg["state_in"] + alg["state_out"]}
+    kb = {names[0]: 0, names[1]: alg["in_bytes"],
+          names[2]: alg["out_bytes"] + alg["state_in"] + alg["state_out"]}
     peak, peak_kind = measured_peaks()
     achieved = kb[names[dom]] / (avg[dom] * 1e-3) / 1e9
     path_achieved = alg["bytes"] / (ms * 1e-3) / 1e9

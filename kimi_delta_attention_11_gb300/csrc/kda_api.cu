@@ -20,8 +20,8 @@ Layout make_layout(int B, int T, int H, int K, int V, int num_seqs, bool packed,
     L.chunk_tab_off = 256;
     L.seq_tab_off = align_up(L.chunk_tab_off + (size_t)L.max_chunks * 16, 256);
     L.inter_off = align_up(L.seq_tab_off + (size_t)L.N * 8, 1024);
-    (void)dt;
-    L.inter_stride = align_up(SimtRecord::floats(K, V) * sizeof(float), 1024);
+    L.inter_stride = use_tc_path(K, V, dt) ? (size_t)TcRecord::bytes
+                                           : align_up(SimtRecord::floats(K, V) * sizeof(float), 1024);
     L.total = L.inter_off + (size_t)L.max_chunks * H * L.inter_stride;
     return L;
 }
@@ -156,9 +156,13 @@ kda_status kda_fwd_profiled(const void* q, const void* k, const void* v, const f
     if (cudaMemsetAsync(ws, 0, 256, s) != cudaSuccess) return KDA_ERR_CUDA;
     if (launch_chunk_index(cu_seqlens, L.N, T, L, ws, s) != cudaSuccess) return KDA_ERR_CUDA;
     if (!mark(1)) return KDA_ERR_CUDA;
-    if (launch_simt(q, k, v, g, beta, scale, initial_state, o, final_state, H, K, V, dtype, L, ws,
-                    s, num_events ? events + 2 : nullptr) != cudaSuccess)
-        return KDA_ERR_CUDA;
+    const cudaError_t e =
+        use_tc_path(K, V, dtype)
+            ? launch_tc(q, k, v, g, beta, scale, initial_state, o, final_state, B, T, H, L, ws, s,
+                        num_events ? events + 2 : nullptr)
+            : launch_simt(q, k, v, g, beta, scale, initial_state, o, final_state, H, K, V, dtype,
+                          L, ws, s, num_events ? events + 2 : nullptr);
+    if (e != cudaSuccess) return KDA_ERR_CUDA;
     return KDA_OK;
 }
 

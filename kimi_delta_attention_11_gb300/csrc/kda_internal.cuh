@@ -44,6 +44,33 @@ struct SimtRecord {
     __host__ __device__ static size_t floats(int K, int V) { return gamma(K, V) + K; }
 };
 
+// Per-(chunk, head) record of the bf16 tensor-core path (K = V = 128).  Every tile is
+// stored as the exact shared-memory image the recurrence kernel feeds to tcgen05
+// (SW128 K-major panels), so that kernel fetches it with plain bulk copies.
+//   wq     [W ; Qg]  2 panels (key 0-63, 64-127) x [128 rows][64]: rows 0-63 W (token),
+//                    rows 64-127 the gated, scaled query.                  32 KB
+//   kbarT  K_bar^T   [128 key rows][64 tokens].                            16 KB
+//   aqk    Aqk       [64 query rows][64 key cols] (zero above the diagonal). 8 KB
+//          (kbarT rows 64-127 followed by aqk form a 128-row A operand whose upper
+//          half only feeds accumulator rows the recurrence has already consumed.)
+//   u      U         [4 value slices][64 tokens][32 values] bf16; the 16-byte chunk q
+//                    of row r is stored at position q ^ (r & 3).             16 KB
+//   gamma  gamma^C   [128] fp32 (decay of the whole chunk per key channel).
+struct TcRecord {
+    static constexpr uint32_t wq = 0;
+    static constexpr uint32_t kbarT = 32768;
+    static constexpr uint32_t aqk = 49152;
+    static constexpr uint32_t u = 57344;
+    static constexpr uint32_t gamma = 73728;
+    static constexpr uint32_t bytes = 74752;  // record stride (1024-aligned)
+};
+
+// The bf16 tensor-core path serves K = V = 128; other bf16 shapes and fp32 take the
+// exact CUDA-core path.
+inline bool use_tc_path(int K, int V, kda_dtype dt) {
+    return dt == KDA_DTYPE_BF16 && K == 128 && V == 128;
+}
+
 // 2-D TMA tensor map over a row-major matrix of `outer` rows x `inner` elements
 // (bf16 or fp32), box of box_outer rows x box_inner elements, optional 128-byte swizzle,
 // zero fill outside the tensor.  Returns false if the driver rejects it.
@@ -55,6 +82,10 @@ Layout make_layout(int B, int T, int H, int K, int V, int num_seqs, bool packed,
 // Launchers (return cudaGetLastError() of their launches).
 cudaError_t launch_chunk_index(const int32_t* cu_seqlens, int N, int T, const Layout& L,
                                char* ws, cudaStream_t s);
+cudaError_t launch_tc(const void* q, const void* k, const void* v, const float* g,
+                      const float* beta, float scale, const float* s0, void* o, float* sN, int B,
+                      int T, int H, const Layout& L, char* ws, cudaStream_t s,
+                      void* const* events_after);
 cudaError_t launch_simt(const void* q, const void* k, const void* v, const float* g,
                         const float* beta, float scale, const float* s0, void* o, float* sN,
                         int H, int K, int V, kda_dtype dt, const Layout& L, char* ws,

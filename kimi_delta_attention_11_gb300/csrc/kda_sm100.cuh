@@ -100,6 +100,21 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
     return false;
 }
 
+// As mbar_wait, but also gives up at once when another thread of the CTA has set
+// *abort (after its own wait expired), and sets *abort itself on expiry, so that one
+// expired wait ends every role of the CTA quickly instead of one bound per wait.
+__device__ __forceinline__ bool mbar_wait_abortable(uint64_t* bar, uint32_t parity, int* status,
+                                                    volatile int* abort) {
+    for (uint32_t i = 0; i < kWaitLimit; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (i >= 16) __nanosleep(64);
+    }
+    atomicCAS(status, 0, 6 /* KDA_ERR_DEVICE_TIMEOUT */);
+    *abort = 1;
+    return false;
+}
+
 // ---------------------------------------------------------------------------
 // TMA and bulk copies
 // ---------------------------------------------------------------------------
