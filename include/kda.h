@@ -171,12 +171,14 @@ kda_status kda_get_device_status(const void* workspace, void* stream);
 
 /* Diagnostic: D[128][N] = A[128][K] * B[N][K]^T (bf16 row-major inputs, fp32 row-major
  * output) computed by one CTA with the same tcgen05 MMA, tensor-memory, mbarrier and
- * 128-byte-swizzled operand building blocks as the bf16 kernels.  mode 0 stages A and B
+ * 128-byte-swizzled operand building blocks as the bf16 kernels.  Mode 0 stages A and B
  * with TMA tensor loads, mode 1 writes them from registers with the software swizzle.
  * N in {16, 32, 64, 128, 256}; K a multiple of 16 in [16, 128].  *status (device int,
  * zeroed by the caller) receives KDA_ERR_DEVICE_TIMEOUT if a bounded wait expires.
  * Used by the tests to check the building blocks in isolation; not part of the
- * forward pass. */
+ * forward pass.  Modes 2 and 3 check the MN-major operand form: in mode 2 B is given as
+ * its transpose [K][N] (N >= 64), in mode 3 A is given as its transpose [K][128]; the
+ * result is the same product. */
 kda_status kda_selftest_umma(const void* A, const void* B, float* D, int N, int K, int mode,
                              int* status, void* stream);
 

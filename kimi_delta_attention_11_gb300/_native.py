@@ -191,8 +191,11 @@ def build_chunk_index(cu_seqlens: Optional[torch.Tensor], B: int, T: int,
 def selftest_umma(A: torch.Tensor, B: torch.Tensor, mode: int = 0) -> torch.Tensor:
     """Diagnostic tcgen05 GEMM: returns A[128,K] @ B[N,K]^T in fp32 (synchronises)."""
     lib = load_library()
-    N, K = B.shape
-    D = torch.empty((A.shape[0], N), dtype=torch.float32, device=A.device)
+    if mode == 2:      # B given transposed: [K, N]
+        K, N = B.shape
+    else:
+        N, K = B.shape
+    D = torch.empty((128, N), dtype=torch.float32, device=A.device)
     status = torch.zeros(1, dtype=torch.int32, device=A.device)
     st = lib.kda_selftest_umma(_ptr(A), _ptr(B), _ptr(D), N, K, mode, _ptr(status),
                                _stream_handle(A.device))

@@ -26,7 +26,7 @@ selftest_mma_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_cons
     uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
     const int panels = (K + 63) / 64;
     uint8_t* sa = smem;                                   // panels x [128][64] bf16
-    uint8_t* sb = smem + panels * 128 * 128;              // panels x [N][64] bf16
+    uint8_t* sb = smem + 2 * 128 * 128;                   // B operand (up to 64 KB)
     const int tid = threadIdx.x, warp = tid / 32;
 
     if (warp == 0) tmem_alloc(&tmem_base, tmem_cols);
@@ -63,14 +63,31 @@ selftest_mma_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_cons
                 tma_load_2d(sb + p * N * 128, &tma_b, p * 64, 0, &bar_full);
             }
             ok = mbar_wait(&bar_full, 0, status);
+        } else if (mode == 2) {  // A K-major panels; B given as [K][N]: N/64 atoms [K][64]
+            mbar_arrive_expect_tx(&bar_full, (uint32_t)(panels * 128 * 128 + K * N * 2));
+            for (int p = 0; p < panels; ++p) tma_load_2d(sa + p * 128 * 128, &tma_a, p * 64, 0, &bar_full);
+            for (int a = 0; a < N / 64; ++a) tma_load_2d(sb + a * K * 128, &tma_b, a * 64, 0, &bar_full);
+            ok = mbar_wait(&bar_full, 0, status);
+        } else if (mode == 3) {  // A given as [K][128]: 2 atoms [K][64]; B K-major panels
+            mbar_arrive_expect_tx(&bar_full, (uint32_t)(K * 128 * 2 + panels * N * 128));
+            for (int a = 0; a < 2; ++a) tma_load_2d(sa + a * K * 128, &tma_a, a * 64, 0, &bar_full);
+            for (int p = 0; p < panels; ++p) tma_load_2d(sb + p * N * 128, &tma_b, p * 64, 0, &bar_full);
+            ok = mbar_wait(&bar_full, 0, status);
         }
         if (ok) {
             tc_fence_after();
-            const uint32_t idesc = idesc_bf16(128, (uint32_t)N);
+            const bool a_mn = mode == 3, b_mn = mode == 2;
+            const uint32_t idesc = idesc_bf16(128, (uint32_t)N, a_mn, b_mn);
             for (int ks = 0; ks < K / 16; ++ks) {
                 const int p = ks / 4, kk = ks % 4;
-                const uint64_t ad = desc_sw128(smem_u32(sa + p * 128 * 128 + kk * 32));
-                const uint64_t bd = desc_sw128(smem_u32(sb + p * N * 128 + kk * 32));
+                // K-major: panel p, +32 B per K step.  MN-major: atoms of [K rows][64] at a
+                // stride of K*128 B, +2048 B (two 8-row groups) per K step.
+                const uint64_t ad =
+                    a_mn ? desc_sw128_mn(smem_u32(sa + ks * 2048), (uint32_t)K * 128, 1024)
+                         : desc_sw128(smem_u32(sa + p * 128 * 128 + kk * 32));
+                const uint64_t bd =
+                    b_mn ? desc_sw128_mn(smem_u32(sb + ks * 2048), (uint32_t)K * 128, 1024)
+                         : desc_sw128(smem_u32(sb + p * N * 128 + kk * 32));
                 mma_bf16(tmem, ad, bd, idesc, ks > 0 ? 1u : 0u);
             }
         }
@@ -102,13 +119,19 @@ extern "C" kda_status kda_selftest_umma(const void* A, const void* B, float* D, 
                                         int mode, int* status, void* stream) {
     if (!A || !B || !D || !status) return KDA_ERR_INVALID_ARG;
     if (!(N == 16 || N == 32 || N == 64 || N == 128 || N == 256)) return KDA_ERR_UNSUPPORTED;
-    if (K < 16 || K > 128 || K % 16 != 0 || (mode != 0 && mode != 1)) return KDA_ERR_UNSUPPORTED;
+    if (K < 16 || K > 128 || K % 16 != 0 || mode < 0 || mode > 3) return KDA_ERR_UNSUPPORTED;
+    if (mode == 2 && N < 64) return KDA_ERR_UNSUPPORTED;
     CUtensorMap ta, tb;
-    if (!make_tmap_2d(&ta, A, true, (uint64_t)K, 128, (uint64_t)K * 2, 64, 128, true) ||
-        !make_tmap_2d(&tb, B, true, (uint64_t)K, (uint64_t)N, (uint64_t)K * 2, 64, (uint32_t)N, true))
-        return KDA_ERR_CUDA;
-    const int panels = (K + 63) / 64;
-    const size_t smem = (size_t)panels * (128 + N) * 128 + 1024;
+    const bool a_mn = mode == 3, b_mn = mode == 2;
+    const bool ok_a = a_mn ? make_tmap_2d(&ta, A, true, 128, (uint64_t)K, 256, 64, (uint32_t)K, true)
+                           : make_tmap_2d(&ta, A, true, (uint64_t)K, 128, (uint64_t)K * 2, 64, 128, true);
+    const bool ok_b = b_mn ? make_tmap_2d(&tb, B, true, (uint64_t)N, (uint64_t)K, (uint64_t)N * 2, 64,
+                                          (uint32_t)K, true)
+                           : make_tmap_2d(&tb, B, true, (uint64_t)K, (uint64_t)N, (uint64_t)K * 2, 64,
+                                          (uint32_t)N, true);
+    if (!ok_a || !ok_b) return KDA_ERR_CUDA;
+    // operand area: both readings of the MN-major offsets stay inside these sizes
+    const size_t smem = 2 * 128 * 128 + 256 * 128 * 2 + 1024;
     const uint32_t cols = N < 32 ? 32u : (uint32_t)N;
     cudaFuncSetAttribute(selftest_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     selftest_mma_kernel<<<1, 128, smem, static_cast<cudaStream_t>(stream)>>>(

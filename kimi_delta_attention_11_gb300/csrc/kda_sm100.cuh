@@ -204,13 +204,25 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t addr) {
            ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
-// Instruction descriptor, kind::f16: bf16 A and B (both K-major), fp32 accumulator.
-__host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N) {
-    return (1u << 4)            // D format f32
-           | (1u << 7)          // A format bf16
-           | (1u << 10)         // B format bf16
-           | ((N >> 3) << 17)   // N / 8
-           | ((M >> 4) << 24);  // M / 16
+// Descriptor of a SW128 MN-major operand: atoms of [8*g K-rows][64 MN-elements]
+// (128 B per K-row, 1024 B per 8-row group); `lbo` = byte distance between 64-wide
+// atoms along M/N, `sbo` = byte distance between 8-row groups along K.
+__device__ __forceinline__ uint64_t desc_sw128_mn(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 accumulator; a_mn / b_mn select
+// the MN-major (transposed) form of the operand (bits 15 / 16).
+__host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N, bool a_mn = false,
+                                                  bool b_mn = false) {
+    return (1u << 4)                 // D format f32
+           | (1u << 7)               // A format bf16
+           | (1u << 10)              // B format bf16
+           | ((a_mn ? 1u : 0u) << 15)
+           | ((b_mn ? 1u : 0u) << 16)
+           | ((N >> 3) << 17)        // N / 8
+           | ((M >> 4) << 24);       // M / 16
 }
 
 // Single thread: D[tmem] (+)= A[smem desc] * B[smem desc]^T.

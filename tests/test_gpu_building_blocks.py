@@ -26,3 +26,25 @@ def test_umma_gemm(kda, mode, N, K):
     ref = A.double() @ B.double().T
     err = (D.double() - ref).abs().max().item()
     assert err <= 1e-3 * max(1.0, ref.abs().max().item()), f"max err {err}"
+
+
+@pytest.mark.parametrize("N", [64, 128, 256])
+@pytest.mark.parametrize("K", [16, 64, 128])
+def test_umma_gemm_b_mn_major(kda, N, K):
+    g = torch.Generator(device="cpu").manual_seed(7 * N + K)
+    A = torch.randn((128, K), generator=g).to(torch.bfloat16).cuda()
+    Bt = torch.randn((K, N), generator=g).to(torch.bfloat16).cuda()
+    D = kda.selftest_umma(A, Bt.contiguous(), 2)
+    ref = A.double() @ Bt.double()
+    assert (D.double() - ref).abs().max().item() <= 1e-3 * max(1.0, ref.abs().max().item())
+
+
+@pytest.mark.parametrize("N", [32, 64, 256])
+@pytest.mark.parametrize("K", [16, 64, 128])
+def test_umma_gemm_a_mn_major(kda, N, K):
+    g = torch.Generator(device="cpu").manual_seed(11 * N + K)
+    At = torch.randn((K, 128), generator=g).to(torch.bfloat16).cuda()
+    B = torch.randn((N, K), generator=g).to(torch.bfloat16).cuda()
+    D = kda.selftest_umma(At.contiguous(), B, 3)
+    ref = At.double().T @ B.double().T
+    assert (D.double() - ref).abs().max().item() <= 1e-3 * max(1.0, ref.abs().max().item())
