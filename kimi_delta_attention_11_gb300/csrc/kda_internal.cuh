@@ -45,21 +45,22 @@ struct SimtRecord {
 };
 
 // Per-(chunk, head) record of the bf16 tensor-core path (K = V = 128).  Every tile is
-// stored as the exact shared-memory image the recurrence kernel feeds to tcgen05
-// (SW128 K-major panels), so that kernel fetches it with plain bulk copies.
-//   wq     [W ; Qg]  2 panels (key 0-63, 64-127) x [128 rows][64]: rows 0-63 W (token),
-//                    rows 64-127 the gated, scaled query.                  32 KB
-//   kbarT  K_bar^T   [128 key rows][64 tokens].                            16 KB
-//   aqk    Aqk       [64 query rows][64 key cols] (zero above the diagonal). 8 KB
-//          (kbarT rows 64-127 followed by aqk form a 128-row A operand whose upper
-//          half only feeds accumulator rows the recurrence has already consumed.)
-//   u      U         [4 value slices][64 tokens][32 values] bf16; the 16-byte chunk q
-//                    of row r is stored at position q ^ (r & 3).             16 KB
+// stored as the exact shared-memory image the recurrence kernel feeds to tcgen05 (128-byte
+// swizzled 64-element panels), so that kernel fetches it with plain bulk copies.
+//   wq     [W ; Qg]  2 panels (key 0-63, 64-127) x [128 rows][64], K-major: rows 0-63 W
+//                    (one per token), rows 64-127 the gated, scaled query.    32 KB
+//   aqk    Aqk       [64 query rows][64 key cols], K-major, zero above the diagonal. 8 KB
+//                    (rows 64-127 of panel 1 of wq followed by aqk form a 128-row A
+//                    operand whose upper half only feeds accumulator rows the
+//                    recurrence has already consumed.)
+//   kbar   K_bar     [64 tokens][128 keys] as 2 panels [64][64] (token-major; read by
+//                    the tensor core as the transposed operand K_bar^T).        16 KB
+//   u      U         [64 tokens][128 values] as 2 panels [64][64] (token-major). 16 KB
 //   gamma  gamma^C   [128] fp32 (decay of the whole chunk per key channel).
 struct TcRecord {
     static constexpr uint32_t wq = 0;
-    static constexpr uint32_t kbarT = 32768;
-    static constexpr uint32_t aqk = 49152;
+    static constexpr uint32_t aqk = 32768;
+    static constexpr uint32_t kbar = 40960;
     static constexpr uint32_t u = 57344;
     static constexpr uint32_t gamma = 73728;
     static constexpr uint32_t bytes = 74752;  // record stride (1024-aligned)
