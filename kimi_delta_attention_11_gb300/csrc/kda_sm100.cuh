@@ -115,6 +115,16 @@ __device__ __forceinline__ bool mbar_wait_abortable(uint64_t* bar, uint32_t pari
     return false;
 }
 
+// Named barriers (ids 1..15; 0 is __syncthreads).  bar_arrive does not wait; bar_sync
+// waits until `count` threads (a multiple of 32) have arrived or synced on `id`.  Both
+// order the participating threads' shared-memory accesses like __syncthreads.
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t count) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // TMA and bulk copies
 // ---------------------------------------------------------------------------
