@@ -66,8 +66,9 @@ typedef enum kda_dtype {
  * Packed input (num_seqs > 0 together with a non-null cu_seqlens at call time) needs
  * room for ceil(T/64) + num_seqs - 1 chunks per head; fixed length for B * ceil(T/64).
  * Pass num_seqs = 0 for fixed-length input.  The workspace holds the chunk table, a
- * device status word and the per-chunk intermediates (W, U, gated keys/queries, Aqk,
- * chunk decay) that the intra-chunk kernel hands to the recurrence kernel. */
+ * device status word, the per-chunk intermediates that the intra-chunk kernel hands to
+ * the recurrence kernel (the chunk's affine state map and output operands), and, for
+ * pipelined calls (see kda_fwd), the state handed between chunk ranges. */
 size_t kda_fwd_workspace_bytes(int B, int T, int H, int K, int V, int num_seqs,
                                int chunk_size, kda_dtype dtype);
 
@@ -97,7 +98,17 @@ size_t kda_fwd_workspace_bytes(int B, int T, int H, int K, int V, int num_seqs,
  *
  * Returns KDA_OK when all launches were enqueued.  Results are deterministic: the
  * same inputs give bit-identical outputs, and o at token t does not depend on any
- * input of a later token of the same sequence. */
+ * input of a later token of the same sequence.
+ *
+ * Schedule.  The bf16 K = V = 128 path on fixed-length input with at most 128
+ * (sequence, head) chains runs pipelined: the chunks of every sequence are cut into
+ * ranges, and the intra-chunk kernel of the next range runs on `stream` while the
+ * recurrence of the current one runs on a second stream of the library (created once
+ * per device with the events it needs; no device memory is allocated).  The second
+ * stream forks from and joins back into `stream` through events, so the call stays
+ * ordered on `stream` and can be captured into a CUDA graph.  Every other case launches
+ * each kernel once over the whole problem.  kda_fwd_launch_count gives the number of
+ * kernel launches. */
 kda_status kda_fwd(const void* q, const void* k, const void* v, const float* g,
                    const float* beta, float scale, int chunk_size,
                    const float* initial_state, const int32_t* cu_seqlens, int num_seqs,
@@ -110,7 +121,9 @@ kda_status kda_fwd(const void* q, const void* k, const void* v, const float* g,
  * after stage i, for the stages in order: 1 chunk index, 2 intra-chunk kernel,
  * 3 recurrence/output kernel.  num_events must be 0 (then this is kda_fwd) or at
  * least 4 (KDA_ERR_INVALID_ARG otherwise).  A stage with nothing to do (T == 0)
- * still gets its event recorded. */
+ * still gets its event recorded.  With events the kernels always run back to back on
+ * `stream`, one launch each over the whole problem (never the pipelined schedule), so
+ * that each stage is one kernel's time; results are identical. */
 kda_status kda_fwd_profiled(const void* q, const void* k, const void* v, const float* g,
                             const float* beta, float scale, int chunk_size,
                             const float* initial_state, const int32_t* cu_seqlens,
@@ -181,6 +194,12 @@ kda_status kda_get_device_status(const void* workspace, void* stream);
  * result is the same product. */
 kda_status kda_selftest_umma(const void* A, const void* B, float* D, int N, int K, int mode,
                              int* status, void* stream);
+
+/* Number of kernel launches kda_fwd makes for these sizes (chunk index, intra-chunk and
+ * recurrence kernels; pipelined calls launch the last two once per chunk range), or -1
+ * for sizes kda_fwd rejects. */
+int kda_fwd_launch_count(int B, int T, int H, int K, int V, int num_seqs, int chunk_size,
+                         kda_dtype dtype);
 
 /* Version of this ABI (major * 100 + minor). */
 int kda_abi_version(void);

@@ -53,6 +53,7 @@ _SIGNATURES = {
     "kda_status_string": (ctypes.c_char_p, [_i]),
     "kda_get_device_status": (_i, [_vp, _vp]),
     "kda_abi_version": (_i, []),
+    "kda_fwd_launch_count": (_i, [_i, _i, _i, _i, _i, _i, _i, _i]),
 }
 
 
@@ -104,6 +105,16 @@ def workspace_bytes(B: int, T: int, H: int, K: int, V: int, num_seqs: int = 0,
     return int(n)
 
 
+def launch_count(B: int, T: int, H: int, K: int, V: int, num_seqs: int = 0,
+                 dtype: torch.dtype = torch.bfloat16, chunk_size: int = 64) -> int:
+    """Number of kernel launches one kda_fwd makes for these sizes."""
+    n = load_library().kda_fwd_launch_count(B, T, H, K, V, num_seqs, chunk_size,
+                                            DTYPE_CODES[dtype])
+    if n < 0:
+        raise KdaError(1, "kda_fwd_launch_count")
+    return int(n)
+
+
 def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
         beta: torch.Tensor, scale: Optional[float] = None,
         initial_state: Optional[torch.Tensor] = None,
@@ -118,7 +129,8 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
     int32 [N+1] (then B == 1).  Returns (o [B,T,H,V] in q.dtype, final_state [N,H,K,V]
     fp32 or None).  ``workspace``/``out``/``final_state`` may be passed to reuse memory.
     ``events``: optional list of >= 4 ``torch.cuda.Event`` recorded around the stages
-    (chunk index, intra-chunk kernel, recurrence kernel) for per-kernel timing.
+    (chunk index, intra-chunk kernel, recurrence kernel) for per-kernel timing; with
+    events the kernels run back to back, one launch each (see include/kda.h).
     """
     lib = load_library()
     B, T, H, K = q.shape

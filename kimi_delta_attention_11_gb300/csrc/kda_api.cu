@@ -23,6 +23,20 @@ Layout make_layout(int B, int T, int H, int K, int V, int num_seqs, bool packed,
     L.inter_stride = use_tc_path(K, V, dt) ? (size_t)TcRecord::bytes
                                            : align_up(SimtRecord::floats(K, V) * sizeof(float), 1024);
     L.total = L.inter_off + (size_t)L.max_chunks * H * L.inter_stride;
+    // Pipelining pays when the recurrence has few, long chains (its ordered chunk steps,
+    // not the SM count, set its time): fixed-length input, at most 128 (sequence, head)
+    // chains and at least 512 chunks per sequence (measured on GB300: a 6 % gain at
+    // 2048 chunks per sequence, a loss at 64, where the recurrence kernel's CTAs, which
+    // need a whole SM each, wait for the next range's intra-chunk CTAs to drain).
+    // Ranges of 32 chunks; a ring of 3 ranges of records so the intra-chunk kernel can
+    // run up to 2 ranges ahead.
+    if (use_tc_path(K, V, dt) && !packed && (long long)B * H <= 128 && nct >= kPipeMinChunks) {
+        L.span = 32;
+        L.ranges = (int)((nct + L.span - 1) / L.span);
+        L.ring = 3;
+        L.carry_off = align_up(L.total, 1024);
+        L.total = L.carry_off + (size_t)B * H * K * V * sizeof(float);
+    }
     return L;
 }
 
@@ -76,7 +90,16 @@ kda_status check_device() {
 
 extern "C" {
 
-int kda_abi_version(void) { return 100; }
+int kda_abi_version(void) { return 101; }
+
+int kda_fwd_launch_count(int B, int T, int H, int K, int V, int num_seqs, int chunk_size,
+                         kda_dtype dtype) {
+    const bool packed = num_seqs > 0;
+    if (check_sizes(B, T, H, K, V, num_seqs, packed, chunk_size, dtype) != KDA_OK) return -1;
+    const Layout L = make_layout(B, T, H, K, V, num_seqs, packed, dtype);
+    if (use_tc_path(K, V, dtype) && L.span > 0) return 1 + 2 * L.ranges;
+    return 1 + (L.max_chunks > 0 ? 1 : 0) + (L.N > 0 ? 1 : 0);
+}
 
 const char* kda_status_string(int status) {
     switch (status) {

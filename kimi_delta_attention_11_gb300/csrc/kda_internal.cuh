@@ -11,6 +11,7 @@
 namespace kda {
 
 constexpr int kChunk = 64;  // chunk size C: the production path fixes C = 64
+constexpr int kPipeMinChunks = 512;  // chunks per sequence from which calls are pipelined
 
 // Byte layout of the caller's workspace.
 //   [0, 4)       int32 device status word (0 = ok, else a kda_status)
@@ -18,6 +19,7 @@ constexpr int kChunk = 64;  // chunk size C: the production path fixes C = 64
 //   chunk table  int4 per chunk   {sequence, first token, length, index in sequence}
 //   seq table    int2 per sequence {first chunk, number of chunks}
 //   inter        per (chunk, head) intermediates of the intra-chunk stage
+//   carry        (pipelined calls) fp32 [N][H][K][V] state handed between chunk ranges
 struct Layout {
     size_t status_off = 0;
     size_t count_off = 16;
@@ -25,9 +27,24 @@ struct Layout {
     size_t seq_tab_off = 0;
     size_t inter_off = 0;
     size_t inter_stride = 0;  // bytes per (chunk, head)
+    size_t carry_off = 0;
     size_t total = 0;
     long long max_chunks = 0;
     int N = 0;
+    // Pipelined schedule (bf16 tensor-core path, fixed-length input with few chains):
+    // the chunks of every sequence are cut into ranges of `span`; the intra-chunk kernel
+    // of range r + 1 runs on the caller's stream while the recurrence of range r runs on
+    // a second stream.  span == 0: one launch of each kernel over the whole problem.
+    int span = 0, ranges = 0, ring = 0;
+};
+
+// Chunk range of one kernel launch: chunks j0 <= j < j0 + span of every sequence
+// (j = index within the sequence); span == 0 means all chunks.  carry: the state buffer
+// between ranges (pipelined calls only).
+struct RangeArgs {
+    int j0 = 0;
+    int span = 0;
+    float* carry = nullptr;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -47,21 +64,26 @@ struct SimtRecord {
 // Per-(chunk, head) record of the bf16 tensor-core path (K = V = 128).  Every tile is
 // stored as the exact shared-memory image the recurrence kernel feeds to tcgen05 (128-byte
 // swizzled 64-element panels), so that kernel fetches it with plain bulk copies.
+//   u1     U, values 64-127: [64 tokens][64] token-major.                         8 KB
 //   wq     [W ; Qg]  2 panels (key 0-63, 64-127) x [128 rows][64], K-major: rows 0-63 W
 //                    (one per token), rows 64-127 the gated, scaled query.    32 KB
 //   aqk    Aqk       [64 query rows][64 key cols], K-major, zero above the diagonal. 8 KB
 //                    (rows 64-127 of panel 1 of wq followed by aqk form a 128-row A
 //                    operand whose upper half only feeds accumulator rows the
 //                    recurrence has already consumed.)
-//   kbar   K_bar     [64 tokens][128 keys] as 2 panels [64][64] (token-major; read by
-//                    the tensor core as the transposed operand K_bar^T).        16 KB
-//   u      U         [64 tokens][128 values] as 2 panels [64][64] (token-major). 16 KB
+//   kb0, kb1  K_bar  keys 0-63 / 64-127: [64 tokens][64] token-major (read by the tensor
+//                    core as the transposed operand K_bar^T).                   16 KB
+//   u0     U, values 0-63.                                                       8 KB
 //   gamma  gamma^C   [128] fp32 (decay of the whole chunk per key channel).
+// The recurrence kernel's CTA for value slice s fetches one contiguous run per chunk:
+// [u1, u0) for s = 1 and [wq, gamma) for s = 0 (one large copy beats several small ones).
 struct TcRecord {
-    static constexpr uint32_t wq = 0;
-    static constexpr uint32_t aqk = 32768;
-    static constexpr uint32_t kbar = 40960;
-    static constexpr uint32_t u = 57344;
+    static constexpr uint32_t u1 = 0;
+    static constexpr uint32_t wq = 8192;
+    static constexpr uint32_t aqk = 40960;
+    static constexpr uint32_t kb0 = 49152;
+    static constexpr uint32_t kb1 = 57344;
+    static constexpr uint32_t u0 = 65536;
     static constexpr uint32_t gamma = 73728;
     static constexpr uint32_t bytes = 74752;  // record stride (1024-aligned)
 };

@@ -14,19 +14,21 @@
 //       blocks stacked to M = 128) and the block's 16 scaled query rows and 16
 //       beta-scaled key rows the N side (N = 64 for two blocks); two rounds share one
 //       operand buffer.
-//   a4  (I + L)^{-1} by blocked forward substitution in fp32 (16 x 16 diagonal blocks,
-//       then three levels of block products); [W | U] = (I + L)^{-1} [D_beta K+ | D_beta V]
-//       by one M 128 x N 256 x K 64 MMA whose B operand is the k and v tiles rescaled in
-//       place (token-major, read as an MN-major operand) (Tokamax design doc Eq. (6)-(7)).
-//       Also K_bar = k 2^{G_C - G} and the gated, scaled query (9.1.5).
+//   a4  (I + L)^{-1} in fp32 on CUDA cores from 16 x 16 blocks: D = inverses of the
+//       diagonal blocks, J = D F (F the blocks below the diagonal), X = (I + J)^{-1} by
+//       block forward substitution, (I + L)^{-1} = X D; each block product is computed a
+//       column per thread with the left factor's rows read as broadcast 16-byte loads.
+//       [W | U] = (I + L)^{-1} [D_beta K+ | D_beta V] by one M 128 x N 256 x K 64 MMA
+//       whose B operand is the k and v tiles rescaled in place (token-major, read as an
+//       MN-major operand) (Tokamax design doc Eq. (6)-(7)).  K_bar = k 2^{G_C - G} and
+//       the gated, scaled query Qg (9.1.5).
 //   The results form one record per (chunk, head) (TcRecord), written as tensor-core
-//   operand images.  Every product is computed from a thread's own rows and stored as
-//   16-byte chunks; nothing is transposed through scalar stores.
+//   operand images.
 //
-// kda_h_o_tc: one CTA (4 warps) per (sequence, head, 64-column slice of V): the ordered
-//   chunk recurrence (Eq. (8)) fused with the output (Eq. (9)).  Records are double-
-//   buffered by bulk copies; the state slice lives in fp32 registers (thread d owns key
-//   row d) and is written as a bf16 operand tile each chunk.  Per chunk:
+// kda_h_o_tc: one CTA (8 epilogue warps + 1 issuer warp) per (sequence, head, 64-column
+//   slice of V): the ordered chunk recurrence (Eq. (8)) fused with the output (Eq. (9)).
+//   The state slice lives in fp32 registers (thread (d, half) owns 32 columns of key row
+//   d) and is written as a bf16 operand tile each chunk.  Per chunk:
 //     MMA1  D1 = [W ; Qg] S                              (M 128, N 64, K 128)
 //     ep1   V_new = U - W S                               (D1 rows 0-63)
 //     MMA3  D3 = K_bar^T V_new                            (M 128 keys, N 64, K 64)
@@ -35,9 +37,13 @@
 //   MMA3 is issued before MMA2 so that the state update, the only step the next chunk
 //   waits for, does not wait for the output product; D1 alternates between two TMEM
 //   buffers and each chunk's output rows are read while the next chunk's MMA1 runs.
-//   A fifth warp issues the record copies and every MMA; it meets the epilogue warps at
-//   named barriers, so no epilogue thread is held up by MMA issue.  Records run through
-//   a ring of three stages so each copy has two chunk steps to arrive.
+//   An issuer warp issues the record copies and every MMA and meets the epilogue warps at
+//   named barriers.  Records run through a ring of three stages, one bulk copy each, so
+//   each copy has two chunk steps to arrive.  Every tcgen05 product here reads both
+//   operands from shared memory, whose bandwidth (128 B per cycle) bounds it: the
+//   chained products are kept to the two that the method needs.
+#include <mutex>
+
 #include "kda_internal.cuh"
 #include "kda_sm100.cuh"
 
@@ -117,35 +123,57 @@ struct IntraMap {
     // factor tables inside FAC after the scan: P0 [4][128] = 2^{G_16b},
     // X [6][128] = 2^{G_16b - G_16b'} (b' < b), C [4][128] = 2^{G_63 - G_16b}
     static constexpr uint32_t P0 = FAC, X = FAC + 2048, CF = FAC + 5120;
-    // reuse after the relation MMAs
-    static constexpr uint32_t AF = RA, LF = RA + 16384;  // Aqk, L fp32 [64][64]
-    static constexpr uint32_t IF = RB;                   // (I + L)^{-1} fp32 [64][64]
+    // after the relation MMAs
+    static constexpr uint32_t AQS = RA;                  // Aqk bf16 [64][64] K-major
+    static constexpr uint32_t LF = RA + 8192;            // L fp32 [64][kLs]
+    static constexpr uint32_t DB = RB;                   // D blocks fp32 [4][16][kBs]
+    static constexpr uint32_t JB = RB + 4 * 1280;        // J blocks fp32 [6][16][kBs]
+    static constexpr uint32_t XB = MISC;                 // X20, X31, X30, scratch [4][16][kBs]
     static constexpr uint32_t AIA = RB + 16384;          // (I + L)^{-1} bf16 [128][64]
-    static constexpr uint32_t WST = KT, UST = VT;        // after the W/U MMA
+    // after the W/U MMA
+    static constexpr uint32_t WST = KT, UST = VT;        // W, U staging (token-major)
 };
 constexpr size_t kIntraSmem = IntraMap::END + 1024;  // + alignment slack
+// Row strides (floats) of the solve's fp32 tiles, chosen so that the fragment loads of
+// the 16x16 block products hit distinct banks.
+constexpr int kLs = 72, kBs = 20;
+static_assert(IntraMap::LF + 64 * kLs * 4 <= IntraMap::RA + 32768, "L tile overflows");
+static_assert(IntraMap::JB + 6 * 16 * kBs * 4 <= IntraMap::AIA, "J blocks overflow");
+static_assert(4 * 16 * kBs * 4 <= IntraMap::END - IntraMap::MISC, "X blocks overflow");
 
 __global__ void __launch_bounds__(kIntraThreads, 2)
 kda_intra_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
              const float* __restrict__ beta, float scale, int H, const int4* __restrict__ chunk_tab,
-             const int* __restrict__ count, long long max_chunks, uint8_t* __restrict__ records,
-             int* __restrict__ status) {
+             const int2* __restrict__ seq_tab, const int* __restrict__ count, long long max_chunks,
+             RangeArgs ra, uint8_t* __restrict__ records, int* __restrict__ status) {
     using M = IntraMap;
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t bar_tma, bar_rel, bar_wu;
     __shared__ uint32_t tmem_base;
     __shared__ int s_abort;
 
-    // chunks run from the last to the first so that the records of early chunks, which
-    // the recurrence reads first, are the most recently written (still in L2)
     const long long blk = blockIdx.x;
     const int h = (int)(blk % H);
-    const long long c = max_chunks - 1 - blk / H;
-    if (c >= *count) return;
+    long long c, slot;
+    if (ra.span == 0) {
+        // whole problem: chunks from the last to the first, so that the records of early
+        // chunks, which the recurrence reads first, are the most recently written
+        c = max_chunks - 1 - blk / H;
+        if (c >= *count) return;
+        slot = c;
+    } else {
+        // chunks j0 <= j < j0 + span of every sequence (j = index within the sequence)
+        const long long rest = blk / H;
+        const int jj = (int)(rest % ra.span), n = (int)(rest / ra.span);
+        const int2 sq = seq_tab[n];
+        if (ra.j0 + jj >= sq.y) return;
+        c = sq.x + ra.j0 + jj;
+        slot = (long long)n * ra.span + jj;
+    }
     const int4 ent = chunk_tab[c];
     const int t0 = ent.y, len = ent.z;
-    uint8_t* rec = records + ((size_t)c * H + h) * TcRecord::bytes;
+    uint8_t* rec = records + ((size_t)slot * H + h) * TcRecord::bytes;
 
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -318,8 +346,8 @@ kda_intra_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 }
                 sts128(sm, M::RB + (grp * 2 + P) * 8192 + sw128_chunk(32 + ii, cc), pack8(kp));
                 sts128(sm, a, pack8(kpl));
-                *reinterpret_cast<uint4*>(rec + TcRecord::kbar + P * 8192 + sw128_chunk(i, cc)) =
-                    pack8(kb);
+                *reinterpret_cast<uint4*>(rec + (P ? TcRecord::kb1 : TcRecord::kb0) +
+                                          sw128_chunk(i, cc)) = pack8(kb);
                 // round 0 of relation A: R_0 (rows 0-63) and R_1 (rows 64-127)
                 const uint32_t ra = M::RA + P * 16384;
                 if (b == 0) {
@@ -406,48 +434,51 @@ kda_intra_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     if (*abort_flag) goto teardown;
 
     {
-        // relation epilogue: TMEM lane L = key j (L < 64: rebased for the first block of
-        // the round, L >= 64: for the second); columns 0-31 the round's 32 query rows,
-        // 32-63 its 32 beta-scaled key rows
-        float* AF = reinterpret_cast<float*>(sm + M::AF);
+        // relation epilogue (all 8 warps; warps q and q+4 share TMEM lanes 32q..32q+31,
+        // warps 0-3 take round 0, warps 4-7 round 1).  TMEM lane L = key j (L < 64:
+        // rebased for the first block of the round, L >= 64: for the second); columns
+        // 0-31 the round's 32 query rows, 32-63 its 32 beta-scaled key rows.  Aqk goes
+        // straight to its bf16 operand image, L to fp32 for the solve; masked entries are
+        // exact zeros.
         float* LF = reinterpret_cast<float*>(sm + M::LF);
-        float* IF = reinterpret_cast<float*>(sm + M::IF);
-        if (warp < 4) {
-            const int L = warp * 32 + lane, j = L & 63, hi = L >> 6;
-            for (int ro = 0; ro < 2; ++ro) {
-                // this lane's block b = 2ro + hi: query columns 16hi.., key columns 32+16hi..
-                float vq[16], vk[16];
-                tmem_ld16(tmem_addr(tmem, warp, 64 * ro + 16 * hi), vq);
-                tmem_ld16(tmem_addr(tmem, warp, 64 * ro + 32 + 16 * hi), vk);
-                const int b = 2 * ro + hi;
+        {
+            const int qd = warp & 3, ro = warp >> 2;
+            const int L = qd * 32 + lane, j = L & 63, hi = L >> 6;
+            const int b = 2 * ro + hi;
+            float vq[16], vk[16];
+            tmem_ld16(tmem_addr(tmem, qd, 64 * ro + 16 * hi), vq);
+            tmem_ld16(tmem_addr(tmem, qd, 64 * ro + 32 + 16 * hi), vk);
 #pragma unroll
-                for (int ci = 0; ci < 16; ++ci) {
-                    const int i = 16 * b + ci;
-                    AF[i * 64 + j] = j <= i ? vq[ci] : 0.f;
-                    LF[i * 64 + j] = j < i ? vk[ci] : 0.f;
-                }
+            for (int ci = 0; ci < 16; ++ci) {
+                const int i = 16 * b + ci;
+                *reinterpret_cast<__nv_bfloat16*>(sm + M::AQS + sw128_offset(i, j)) =
+                    __float2bfloat16_rn(j <= i ? vq[ci] : 0.f);
+                LF[i * kLs + j] = j < i ? vk[ci] : 0.f;
             }
-        } else {
-            for (int idx = tid - 128; idx < 4096; idx += 128) IF[idx] = 0.f;
         }
         tc_fence_before();
         __syncthreads();
 
-        // Aqk (bf16) to the record
-        for (int u = tid; u < 512; u += kIntraThreads) {
-            const int i = u >> 3, jc = u & 7;
-            float a[8];
-            ld8f(AF + i * 64 + jc * 8, 0, a);
-            *reinterpret_cast<uint4*>(rec + TcRecord::aqk + sw128_chunk(i, jc)) = pack8(a);
-        }
-        __syncthreads();  // AF is reused as scratch below
-        // a4: (I + L)^{-1} in fp32 by blocks of 16 (Tokamax design doc 4.1.4 uses the same
-        // finite expansion with MXU products).  With D the inverses of the diagonal
-        // blocks and J = D F (F the blocks below the diagonal, J strictly block-lower, so
-        // J^4 = 0): (I + L)^{-1} = (I + J)^{-1} D = (I - J + J^2 - J^3) D.
-        // Stage 1, D: right-looking forward substitution, one column per thread
-        //   (after x_m is final, every later row subtracts L[r][m] x_m).
-        float* JS = reinterpret_cast<float*>(sm + M::AF);  // J [6][16][16] | J^2 [3] | J^3 [1]
+        // a4: (I + L)^{-1} (Tokamax design doc 4.1.4 expands the same block inverse with
+        // MXU products).  L = Lb + F with Lb the strictly lower parts of the 16 x 16
+        // diagonal blocks and F the blocks below them.  With D = (I + Lb)^{-1} (block
+        // diagonal) and J = D F: I + L = (I + Lb)(I + J), so (I + L)^{-1} = (I + J)^{-1} D
+        // = X D, X unit block-lower-triangular with X_i0 = -sum_{k<i} J_ik X_k0 (block
+        // forward substitution).  D in fp32 on CUDA cores; the 16 x 16 block products on
+        // the warp-level tensor-core instruction in TF32 (inputs rounded to 10 mantissa
+        // bits, fp32 accumulation): the result is rounded to bf16 for the W/U product
+        // anyway, 4x coarser.
+        float* DB = reinterpret_cast<float*>(sm + M::DB);
+        float* JB = reinterpret_cast<float*>(sm + M::JB);
+        float* XB = reinterpret_cast<float*>(sm + M::XB);
+        constexpr int kBlk = 16 * kBs;
+        auto put_ai = [&](int r, int cidx, float x) {  // element (r, c) of the bf16 operand
+            *reinterpret_cast<__nv_bfloat16*>(sm + M::AIA + sw128_offset(r, cidx)) =
+                __float2bfloat16_rn(x);
+        };
+        // Stage 1 (warps 0-1): D, one column per thread, right-looking forward
+        // substitution (after x_m is final, every later row subtracts L[r][m] x_m).
+        // Warps 2-7 meanwhile zero the bf16 blocks above the diagonal (192 chunks).
         if (tid < 64) {
             const int bb = tid >> 4, cidx = tid & 15, o = 16 * bb;
             float acc[16];
@@ -457,85 +488,111 @@ kda_intra_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             for (int m = 0; m < 15; ++m)
 #pragma unroll
                 for (int r = m + 1; r < 16; ++r)
-                    acc[r] = fmaf(-LF[(o + r) * 64 + o + m], acc[m], acc[r]);
+                    acc[r] = fmaf(-LF[(o + r) * kLs + o + m], acc[m], acc[r]);
 #pragma unroll
-            for (int r = 0; r < 16; ++r) IF[(o + r) * 64 + o + cidx] = acc[r];
-        }
-        __syncthreads();
-        // block (i, j) below the diagonal: index in J, in pair order (1,0)(2,0)(2,1)(3,0)(3,1)(3,2)
-        const int r16 = (tid >> 4) & 15, c16 = tid & 15;
-        // Stage 2: J_ij = D_i L_ij, six blocks, six elements per thread
-        {
-            float acc[6];
-#pragma unroll
-            for (int pi = 0; pi < 6; ++pi) {
-                const int bi = pi < 1 ? 1 : (pi < 3 ? 2 : 3), bj = pi - pair_index(bi, 0);
-                float a = 0.f;
-#pragma unroll
-                for (int m = 0; m < 16; ++m)
-                    a = fmaf(IF[(16 * bi + r16) * 64 + 16 * bi + m], LF[(16 * bi + m) * 64 + 16 * bj + c16], a);
-                acc[pi] = a;
+            for (int r = 0; r < 16; ++r) {
+                DB[bb * kBlk + r * kBs + cidx] = acc[r];
+                put_ai(o + r, o + cidx, acc[r]);
             }
-#pragma unroll
-            for (int pi = 0; pi < 6; ++pi) JS[pi * 256 + r16 * 16 + c16] = acc[pi];
+        } else {
+            const int t = tid - 64;  // rows 0-15: chunks 2-7; 16-31: 4-7; 32-47: 6-7
+            int r, ch;
+            if (t < 96) { r = t / 6; ch = 2 + t % 6; }
+            else if (t < 160) { r = 16 + (t - 96) / 4; ch = 4 + (t - 96) % 4; }
+            else { r = 32 + (t - 160) / 2; ch = 6 + (t - 160) % 2; }
+            sts128(sm, M::AIA + sw128_chunk(r, ch), make_uint4(0u, 0u, 0u, 0u));
         }
         __syncthreads();
-        // Stage 3: J^2 blocks (2,0) = J21 J10, (3,1) = J32 J21, (3,0) = J31 J10 + J32 J20
-        {
-            const float* J = JS;
-            auto jb = [&](int pi, int r, int c) { return J[pi * 256 + r * 16 + c]; };
-            float a20 = 0.f, a31 = 0.f, a30 = 0.f;
+
+        // Block products: one warp per 16 x 16 result, acc[nt] the two m16n8 tiles.
+        // Pair order of the blocks below the diagonal: (1,0) (2,0) (2,1) (3,0) (3,1) (3,2).
+        const int fg = lane >> 2, ft = lane & 3;  // fragment row group / thread in group
+        auto pair_bi = [](int pi) { return pi < 1 ? 1 : (pi < 3 ? 2 : 3); };
+        // acc += sa * A B  (A, B fp32 16 x 16 with row strides lda, ldb)
+        auto blk_mma = [&](float (&acc)[2][4], const float* A, int lda, const float* B, int ldb,
+                           float sa) {
 #pragma unroll
-            for (int m = 0; m < 16; ++m) {
-                a20 = fmaf(jb(2, r16, m), jb(0, m, c16), a20);
-                a31 = fmaf(jb(5, r16, m), jb(2, m, c16), a31);
-                a30 = fmaf(jb(4, r16, m), jb(0, m, c16), a30);
-                a30 = fmaf(jb(5, r16, m), jb(1, m, c16), a30);
-            }
-            JS[1536 + 0 * 256 + r16 * 16 + c16] = a20;
-            JS[1536 + 1 * 256 + r16 * 16 + c16] = a31;
-            JS[1536 + 2 * 256 + r16 * 16 + c16] = a30;
-        }
-        __syncthreads();
-        // Stage 4: J^3 block (3,0) = J32 (J^2)20
-        {
-            float a = 0.f;
+            for (int ks = 0; ks < 2; ++ks) {
+                uint32_t a[4];
+                a[0] = f32_to_tf32(sa * A[fg * lda + 8 * ks + ft]);
+                a[1] = f32_to_tf32(sa * A[(fg + 8) * lda + 8 * ks + ft]);
+                a[2] = f32_to_tf32(sa * A[fg * lda + 8 * ks + ft + 4]);
+                a[3] = f32_to_tf32(sa * A[(fg + 8) * lda + 8 * ks + ft + 4]);
 #pragma unroll
-            for (int m = 0; m < 16; ++m)
-                a = fmaf(JS[5 * 256 + r16 * 16 + m], JS[1536 + m * 16 + c16], a);
-            JS[2304 + r16 * 16 + c16] = a;
-        }
-        __syncthreads();
-        // Stage 5: Ainv_ij = (-J + J^2 - J^3)_ij D_j for the six blocks below the diagonal
-        {
-            float acc[6];
-#pragma unroll
-            for (int pi = 0; pi < 6; ++pi) {
-                const int bi = pi < 1 ? 1 : (pi < 3 ? 2 : 3), bj = pi - pair_index(bi, 0);
-                const int k2 = (bi == 2 && bj == 0) ? 0 : (bi == 3 && bj == 1) ? 1 : (bi == 3 && bj == 0) ? 2 : -1;
-                float a = 0.f;
-#pragma unroll
-                for (int m = 0; m < 16; ++m) {
-                    float mv = -JS[pi * 256 + r16 * 16 + m];
-                    if (k2 >= 0) mv += JS[1536 + k2 * 256 + r16 * 16 + m];
-                    if (pi == 3) mv -= JS[2304 + r16 * 16 + m];
-                    a = fmaf(mv, IF[(16 * bj + m) * 64 + 16 * bj + c16], a);
+                for (int nt = 0; nt < 2; ++nt) {
+                    uint32_t b[2];
+                    b[0] = f32_to_tf32(B[(8 * ks + ft) * ldb + 8 * nt + fg]);
+                    b[1] = f32_to_tf32(B[(8 * ks + ft + 4) * ldb + 8 * nt + fg]);
+                    mma_tf32_16x8x8(acc[nt], a, b);
                 }
-                acc[pi] = a;
             }
+        };
+        // accumulator tile <-> a [16][kBs] block (element (r, c) of tile nt, slot e:
+        // r = fg + 8 (e >> 1), c = 8 nt + 2 ft + (e & 1))
+        auto acc_load = [&](float (&acc)[2][4], const float* C, float sc) {
 #pragma unroll
-            for (int pi = 0; pi < 6; ++pi) {
-                const int bi = pi < 1 ? 1 : (pi < 3 ? 2 : 3), bj = pi - pair_index(bi, 0);
-                IF[(16 * bi + r16) * 64 + 16 * bj + c16] = acc[pi];
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    acc[nt][e] = sc * C[(fg + 8 * (e >> 1)) * kBs + 8 * nt + 2 * ft + (e & 1)];
+        };
+        auto acc_store = [&](const float (&acc)[2][4], float* C) {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr)
+                    *reinterpret_cast<float2*>(C + (fg + 8 * hr) * kBs + 8 * nt + 2 * ft) =
+                        make_float2(acc[nt][2 * hr], acc[nt][2 * hr + 1]);
+        };
+        // Stage 2 (warps 0-5, warp = pair): J_ij = D_i F_ij.
+        if (warp < 6) {
+            const int pi = warp, bi = pair_bi(pi), bj = pi - pair_index(bi, 0);
+            float acc[2][4] = {};
+            blk_mma(acc, DB + bi * kBlk, kBs, LF + (16 * bi) * kLs + 16 * bj, kLs, 1.f);
+            acc_store(acc, JB + pi * kBlk);
+        }
+        __syncthreads();
+        // Stage 3 (warps 0-2): X20 = J21 J10 - J20, X31 = J32 J21 - J31,
+        // X30 = J31 J10 + J32 J20 - J30 - J32 (J21 J10) (warp 2, through a scratch block).
+        if (warp < 3) {
+            float acc[2][4];
+            const float* J = JB;
+            if (warp == 0) {
+                acc_load(acc, J + 1 * kBlk, -1.f);
+                blk_mma(acc, J + 2 * kBlk, kBs, J + 0 * kBlk, kBs, 1.f);
+                acc_store(acc, XB + 0 * kBlk);
+            } else if (warp == 1) {
+                acc_load(acc, J + 4 * kBlk, -1.f);
+                blk_mma(acc, J + 5 * kBlk, kBs, J + 2 * kBlk, kBs, 1.f);
+                acc_store(acc, XB + 1 * kBlk);
+            } else {
+                float y[2][4] = {};
+                blk_mma(y, J + 2 * kBlk, kBs, J + 0 * kBlk, kBs, 1.f);  // J21 J10
+                acc_store(y, XB + 3 * kBlk);
+                acc_load(acc, J + 3 * kBlk, -1.f);
+                blk_mma(acc, J + 4 * kBlk, kBs, J + 0 * kBlk, kBs, 1.f);
+                blk_mma(acc, J + 5 * kBlk, kBs, J + 1 * kBlk, kBs, 1.f);
+                __syncwarp();
+                blk_mma(acc, J + 5 * kBlk, kBs, XB + 3 * kBlk, kBs, -1.f);
+                acc_store(acc, XB + 2 * kBlk);
             }
         }
         __syncthreads();
-        // (I + L)^{-1} as the bf16 A operand of the W/U product (rows 64-127 unused)
-        for (int u = tid; u < 512; u += kIntraThreads) {
-            const int r = u >> 3, jc = u & 7;
-            float a[8];
-            ld8f(IF + r * 64 + jc * 8, 0, a);
-            sts128(sm, M::AIA + sw128_chunk(r, jc), pack8(a));
+        // Stage 5 (warps 0-5, warp = pair): (I + L)^{-1}_ij = X_ij D_j, written as bf16;
+        // X_10 = -J10, X_21 = -J21, X_32 = -J32.
+        if (warp < 6) {
+            const int pi = warp, bi = pair_bi(pi), bj = pi - pair_index(bi, 0);
+            const float* xl = pi == 1 ? XB : (pi == 4 ? XB + kBlk : (pi == 3 ? XB + 2 * kBlk : JB + pi * kBlk));
+            const float sgn = (pi == 0 || pi == 2 || pi == 5) ? -1.f : 1.f;
+            float acc[2][4] = {};
+            blk_mma(acc, xl, kBs, DB + bj * kBlk, kBs, sgn);
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr)
+                    *reinterpret_cast<uint32_t*>(sm + M::AIA +
+                                                 sw128_offset(16 * bi + fg + 8 * hr, 16 * bj + 8 * nt + 2 * ft)) =
+                        pack_bf16x2(acc[nt][2 * hr], acc[nt][2 * hr + 1]);
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -543,7 +600,8 @@ kda_intra_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     }
 
     // [W | U] = (I+L)^{-1} [D_beta K+ | D_beta V]: M 128 (tokens, 64 used), N 256, K 64;
-    // B is the token-major k|v tiles (4 atoms of 64 columns, 8 KB apart)
+    // B is the token-major k|v tiles (4 atoms of 64 columns, 8 KB apart).  The same thread
+    // then stores Aqk to the record, overlapping the product.
     if (tid == 0) {
         tc_fence_after();
         const uint32_t idesc = idesc_bf16(128, 256, false, true);
@@ -551,13 +609,16 @@ kda_intra_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             mma_bf16(tmem, desc_sw128(sb + M::AIA + kk * 32),
                      desc_sw128_mn(sb + M::KT + kk * 2048, 8192, 1024), idesc, kk > 0 ? 1u : 0u);
         mma_commit(&bar_wu);
+        bulk_store(rec + TcRecord::aqk, sm + M::AQS, 8192);
+        bulk_commit();
     }
     mbar_wait_abortable(&bar_wu, 0, status, abort_flag);
     tc_fence_after();
     __syncthreads();
     if (*abort_flag) goto teardown;
 
-    // W rows (warps 0,1) and U rows (warps 4,5) into staging images of the record tiles
+    // W rows (warps 0,1) and U rows (warps 4,5) into token-major staging tiles, then to
+    // the record by bulk copies (whole lines, where per-thread row stores would not be)
     if (warp == 0 || warp == 1 || warp == 4 || warp == 5) {
         const int r = (warp & 1) * 32 + lane;
         const uint32_t dst = warp < 4 ? M::WST : M::UST;
@@ -580,9 +641,10 @@ kda_intra_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     if (tid == 0) {
         bulk_store(rec + TcRecord::wq, sm + M::WST, 8192);
         bulk_store(rec + TcRecord::wq + 16384, sm + M::WST + 8192, 8192);
-        bulk_store(rec + TcRecord::u, sm + M::UST, 16384);
+        bulk_store(rec + TcRecord::u0, sm + M::UST, 8192);
+        bulk_store(rec + TcRecord::u1, sm + M::UST + 8192, 8192);
         bulk_commit();
-        // only the shared-memory source must outlive the copies; the stores themselves
+        // only the shared-memory sources must outlive the copies; the stores themselves
         // are complete for any later kernel on the stream
         bulk_wait_read_all();
     }
@@ -598,32 +660,35 @@ teardown:
 // ---------------------------------------------------------------------------
 
 constexpr int kVT = 64;                   // value columns per CTA
-constexpr int kHoThreads = 160;           // 4 epilogue warps (thread d <-> TMEM lane d <->
-                                          // key row d of S) + 1 issuer warp
-constexpr uint32_t kStageBytes = 66560;   // wq|aqk|kbar 56K | U panel 8K | gamma 512 (65 KB)
-constexpr uint32_t kStTx = 57344 + 8192 + 512;
+constexpr int kEpiWarps = 8;              // warp w: TMEM lanes 32 (w % 4).., value columns
+                                          // 32 (w / 4).. of the slice
+constexpr int kHoThreads = (kEpiWarps + 1) * 32;  // + 1 issuer warp
 constexpr int kStages = 3;                // record ring depth: copies run 2 chunk steps ahead
+constexpr uint32_t kStage = 65536;        // one contiguous run of the record per chunk
 // named barriers between the epilogue warps and the issuer warp
-constexpr uint32_t kBarVnew = 1;          // warps 0-1 -> issuer: V_new tile written
-constexpr uint32_t kBarState = 2;         // warps 0-3 -> issuer: S tile written, D1/D3 read
+constexpr uint32_t kBarVnew = 1;          // warps of lanes 0-63 -> issuer: V_new tile written
+constexpr uint32_t kBarState = 2;         // all epilogue warps -> issuer: S tile written
+constexpr uint32_t kVnewCount = 4 * 32 + 32;
 
 struct HoMap {
-    static constexpr uint32_t ST = kStages * kStageBytes;  // S tile bf16 [128 keys][64 values]
-    static constexpr uint32_t VN = ST + 16384;              // V_new tile bf16 [64 tokens][64 values]
+    static constexpr uint32_t ST = kStages * kStage;  // S tile bf16 [128 keys][64 values]
+    static constexpr uint32_t VN = ST + 16384;         // V_new tile bf16 [64 tokens][64 values]
     static constexpr uint32_t END = VN + 8192;
-    // inside a stage
-    static constexpr uint32_t WQ = 0, AQK = 32768, KB = 40960, U = 57344, GAM = 65536;
 };
 constexpr size_t kHoSmem = HoMap::END + 1024;
+static_assert(kHoSmem <= 232448, "recurrence kernel exceeds the shared-memory limit");
+static_assert(TcRecord::u1 == 0 && TcRecord::u0 == kStage && TcRecord::gamma == kStage + 8192 &&
+                  TcRecord::aqk == TcRecord::wq + 32768 && TcRecord::kb1 == TcRecord::kb0 + 8192,
+              "record layout assumed by the recurrence kernel");
 
 __global__ void __launch_bounds__(kHoThreads, 1)
 kda_h_o_tc(const uint8_t* __restrict__ records, const int4* __restrict__ chunk_tab,
-           const int2* __restrict__ seq_tab, long long max_chunks, const float* __restrict__ s0,
-           __nv_bfloat16* __restrict__ o, float* __restrict__ sN, int H,
-           int* __restrict__ status) {
+           const int2* __restrict__ seq_tab, long long max_chunks, RangeArgs ra,
+           const float* __restrict__ s0, __nv_bfloat16* __restrict__ o, float* __restrict__ sN,
+           int H, int* __restrict__ status) {
     using M = HoMap;
     extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t full[kStages], bar_m1, bar_m3, bar_m2;
+    __shared__ uint64_t full[kStages], bar_m1, bar_m3, bar_m2[2];
     __shared__ uint32_t tmem_base;
     __shared__ int s_abort;
 
@@ -635,12 +700,30 @@ kda_h_o_tc(const uint8_t* __restrict__ records, const int4* __restrict__ chunk_t
     const uint32_t sb = smem_u32(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int2 sq = seq_tab[n];
-    const long long first = sq.x;
-    int nch = sq.y;
-    if (first + nch > max_chunks) {  // inconsistent cu_seqlens: stop rather than overrun
+    int seq_chunks = sq.y;
+    if ((long long)sq.x + seq_chunks > max_chunks) {  // inconsistent cu_seqlens: stop rather than overrun
         if (tid == 0) atomicCAS(status, 0, (int)KDA_ERR_INVALID_ARG);
-        nch = (int)(max_chunks > first ? max_chunks - first : 0);
+        seq_chunks = (int)(max_chunks > sq.x ? max_chunks - sq.x : 0);
     }
+    // this launch runs chunks lo <= j < hi of the sequence (all of them, or one range of a
+    // pipelined call); the state comes from initial_state (or zeros) at j = 0, else from
+    // the carry buffer, and goes to final_state after the sequence's last chunk, else to
+    // the carry buffer
+    const int lo = ra.span ? ra.j0 : 0;
+    const int hi = ra.span ? min(ra.j0 + ra.span, seq_chunks) : seq_chunks;
+    if (lo >= hi && !(lo == 0 && seq_chunks == 0)) return;  // nothing of this sequence here
+    const int nch = hi > lo ? hi - lo : 0;
+    const long long first = (long long)sq.x + lo;            // global index of chunk lo
+    const long long slot0 = ra.span ? (long long)n * ra.span : first;
+    const float* s_in = lo == 0 ? s0 : ra.carry;
+    float* s_out = hi == seq_chunks ? sN : ra.carry;
+    auto rec_of = [&](int ci) {
+        return records + ((size_t)(slot0 + ci) * H + h) * TcRecord::bytes;
+    };
+    // slice s copies record bytes [cs, cs + kStage): stage offset = record offset - cs
+    const uint32_t cs = slice ? TcRecord::u1 : TcRecord::wq;
+    const uint32_t WQ = TcRecord::wq - cs, AQK = TcRecord::aqk - cs, KB = TcRecord::kb0 - cs;
+    const uint32_t UO = (slice ? TcRecord::u1 : TcRecord::u0) - cs;
 
     if (warp == 0) tmem_alloc(&tmem_base, 256);
     if (tid == 0) {
@@ -648,7 +731,8 @@ kda_h_o_tc(const uint8_t* __restrict__ records, const int4* __restrict__ chunk_t
         for (int i = 0; i < kStages; ++i) mbar_init(&full[i], 1);
         mbar_init(&bar_m1, 1);
         mbar_init(&bar_m3, 1);
-        mbar_init(&bar_m2, 1);
+        mbar_init(&bar_m2[0], 1);
+        mbar_init(&bar_m2[1], 1);
         fence_barrier_init();
     }
     tc_fence_before();
@@ -658,20 +742,15 @@ kda_h_o_tc(const uint8_t* __restrict__ records, const int4* __restrict__ chunk_t
     // (the output); D3: K_bar^T V_new (the state update)
     const uint32_t tmem = tmem_base, D3 = tmem + 128;
     volatile int* abort_flag = &s_abort;
-    const size_t st_off = ((size_t)n * H + h) * 128 * 128 + slice * kVT;
 
-    if (warp == 4) {
+    if (warp == kEpiWarps) {
         // ---- issuer warp: record copies and every MMA (lane 0 issues).  The whole warp
         // runs the loop so that its named-barrier syncs are warp-uniform; every exit
         // decision is made uniform with a warp vote. ----
         auto load = [&](int ci) {  // record of chunk ci into stage ci % kStages (lane 0)
             const int sg = ci % kStages;
-            const uint8_t* rec = records + ((size_t)(first + ci) * H + h) * TcRecord::bytes;
-            uint8_t* st = sm + sg * kStageBytes;
-            mbar_arrive_expect_tx(&full[sg], kStTx);
-            bulk_load(st + M::WQ, rec + TcRecord::wq, 57344, &full[sg]);  // wq, aqk, kbar
-            bulk_load(st + M::U, rec + TcRecord::u + slice * 8192, 8192, &full[sg]);
-            bulk_load(st + M::GAM, rec + TcRecord::gamma, 512, &full[sg]);
+            mbar_arrive_expect_tx(&full[sg], kStage);
+            bulk_load(sm + sg * kStage, rec_of(ci) + cs, kStage, &full[sg]);
         };
         if (lane == 0)
             for (int ci = 0; ci < kStages && ci < nch; ++ci) load(ci);
@@ -682,16 +761,16 @@ kda_h_o_tc(const uint8_t* __restrict__ records, const int4* __restrict__ chunk_t
         const uint64_t dVN = desc_sw128_mn(sb + M::VN, 8192, 1024);
         for (int ci = 0; ci < nch; ++ci) {
             const int sg = ci % kStages;
-            const uint32_t stb = sb + sg * kStageBytes;
+            const uint32_t stb = sb + sg * kStage;
             const uint32_t D1 = tmem + 64 * (ci & 1);
             bool ok = mbar_wait_abortable(&full[sg], (ci / kStages) & 1, status, abort_flag);
             if (!__all_sync(0xffffffffu, ok)) break;
-            named_bar_sync(kBarState, 160);  // S_ci written, D1/D3 of earlier chunks read
+            named_bar_sync(kBarState, kHoThreads);  // S_ci written, D1/D3 of earlier chunks read
             if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
             if (lane == 0) {
                 tc_fence_after();
                 // MMA1: D1 = [W ; Qg] S   (K = 128 keys over two panels)
-                const uint64_t dWQ = desc_sw128(stb + M::WQ);
+                const uint64_t dWQ = desc_sw128(stb + WQ);
                 for (int ks = 0; ks < 8; ++ks)
                     mma_bf16(D1, dWQ + (uint64_t)(((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
                              dS + (uint64_t)((ks * 2048) >> 4), idesc_a, ks > 0 ? 1u : 0u);
@@ -700,149 +779,185 @@ kda_h_o_tc(const uint8_t* __restrict__ records, const int4* __restrict__ chunk_t
             __syncwarp();
             // refill the stage chunk ci-1 used: its MMA2 precedes this MMA1 on the pipe
             if (ci >= 1 && ci - 1 + kStages < nch) {
-                ok = mbar_wait_abortable(&bar_m2, (ci - 1) & 1, status, abort_flag);
+                ok = mbar_wait_abortable(&bar_m2[(ci - 1) & 1], ((ci - 1) >> 1) & 1, status, abort_flag);
                 if (!__all_sync(0xffffffffu, ok)) break;
                 if (lane == 0) load(ci - 1 + kStages);
                 __syncwarp();
             }
-            named_bar_sync(kBarVnew, 96);  // V_new tile written by warps 0-1
+            named_bar_sync(kBarVnew, kVnewCount);  // V_new tile written
             if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
             if (lane == 0) {
                 tc_fence_after();
                 // MMA3 first (it feeds the state): D3 = K_bar^T V_new (K_bar token-major:
                 // MN-major A, 2 atoms 8 KB apart)
-                const uint64_t dKB = desc_sw128_mn(stb + M::KB, 8192, 1024);
+                const uint64_t dKB = desc_sw128_mn(stb + KB, 8192, 1024);
                 for (int kk = 0; kk < 4; ++kk)
                     mma_bf16(D3, dKB + (uint64_t)((kk * 2048) >> 4),
                              dVN + (uint64_t)((kk * 2048) >> 4), idesc_t, kk > 0 ? 1u : 0u);
                 mma_commit(&bar_m3);
                 // MMA2: D1 += [Qg panel-1 rows ; Aqk] V_new  (only rows 64-127 are used)
-                const uint64_t dQA = desc_sw128(stb + M::WQ + 16384 + 8192);
+                const uint64_t dQA = desc_sw128(stb + AQK - 8192);
                 for (int kk = 0; kk < 4; ++kk)
                     mma_bf16(D1, dQA + (uint64_t)((kk * 32) >> 4),
                              dVN + (uint64_t)((kk * 2048) >> 4), idesc_a, 1u);
-                mma_commit(&bar_m2);
+                mma_commit(&bar_m2[ci & 1]);
             }
             __syncwarp();
         }
     } else {
-        // ---- epilogue warps: thread d owns row d of the state slice, fp32 ----
-        const int d = tid;
-        float S[kVT];
+        // ---- epilogue warps: thread (d, half) owns 32 columns of row d of the state
+        // slice, fp32 ----
+        const int qd = warp & 3, half = warp >> 2, d = qd * 32 + lane;
+        const size_t st_off = ((size_t)n * H + h) * 128 * 128 + (size_t)d * 128 + slice * kVT + 32 * half;
+        float S[32];
         {
-            const float4* src = reinterpret_cast<const float4*>(s0 + st_off + (size_t)d * 128);
+            const float4* src = reinterpret_cast<const float4*>(s_in + st_off);
 #pragma unroll
-            for (int x = 0; x < kVT / 4; ++x) {
-                const float4 f = s0 ? src[x] : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int x = 0; x < 8; ++x) {
+                const float4 f = s_in ? src[x] : make_float4(0.f, 0.f, 0.f, 0.f);
                 S[4 * x] = f.x;
                 S[4 * x + 1] = f.y;
                 S[4 * x + 2] = f.z;
                 S[4 * x + 3] = f.w;
             }
         }
-        // S tile: key-major [128][64] bf16 (MN-major B operand), row d = 8 chunks of 16 B
+        // S tile: key-major [128][64] bf16 (MN-major B operand); this thread writes chunks
+        // 4 half .. 4 half + 3 of row d
         auto write_state = [&]() {
 #pragma unroll
-            for (int qd = 0; qd < 8; ++qd) {
+            for (int q4 = 0; q4 < 4; ++q4) {
                 float f[8];
 #pragma unroll
-                for (int m = 0; m < 8; ++m) f[m] = S[qd * 8 + m];
-                sts128(sm, M::ST + sw128_chunk(d, qd), pack8(f));
+                for (int m = 0; m < 8; ++m) f[m] = S[q4 * 8 + m];
+                sts128(sm, M::ST + sw128_chunk(d, 4 * half + q4), pack8(f));
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            named_bar_arrive(kBarState, 160);
+            named_bar_arrive(kBarState, kHoThreads);
         };
-        // output of chunk ci (warps 2 and 3, token = lane index - 64)
+        // output rows of chunk ci (TMEM lanes 64-127: token = lane index - 64)
         auto emit_output = [&](int ci) {
-            if (!__all_sync(0xffffffffu, mbar_wait_abortable(&bar_m2, ci & 1, status, abort_flag)))
+            if (!__all_sync(0xffffffffu, mbar_wait_abortable(&bar_m2[ci & 1], (ci >> 1) & 1, status,
+                                                             abort_flag)))
                 return;
             tc_fence_after();
-            float ov[64];
-            const uint32_t D1 = tmem + 64 * (ci & 1);
-            tmem_ld32(tmem_addr(D1, warp, 0), *reinterpret_cast<float(*)[32]>(ov));
-            tmem_ld32(tmem_addr(D1, warp, 32), *reinterpret_cast<float(*)[32]>(ov + 32));
+            float ov[32];
+            tmem_ld32(tmem_addr(tmem + 64 * (ci & 1), qd, 32 * half), ov);
             const int4 ent = chunk_tab[first + ci];
             const int i = d - 64;
             if (i < ent.z) {
                 uint4* dst = reinterpret_cast<uint4*>(o + ((size_t)(ent.y + i) * H + h) * 128 +
-                                                      slice * kVT);
+                                                      slice * kVT + 32 * half);
 #pragma unroll
-                for (int qd = 0; qd < 8; ++qd) {
+                for (int q4 = 0; q4 < 4; ++q4) {
                     float f[8];
 #pragma unroll
-                    for (int m = 0; m < 8; ++m) f[m] = ov[qd * 8 + m];
-                    dst[qd] = pack8(f);
+                    for (int m = 0; m < 8; ++m) f[m] = ov[q4 * 8 + m];
+                    dst[q4] = pack8(f);
                 }
             }
         };
+        // gamma^C of the next chunks, fetched two chunk steps ahead
+        auto gamma_of = [&](int ci) {
+            return ci < nch ? reinterpret_cast<const float*>(rec_of(ci) + TcRecord::gamma)[d] : 0.f;
+        };
+        float gam0 = gamma_of(0), gam1 = gamma_of(1);
         write_state();
         for (int ci = 0; ci < nch; ++ci) {
             const int sg = ci % kStages;
-            const uint32_t stb = sb + sg * kStageBytes;
-            const uint8_t* st = sm + sg * kStageBytes;
             const uint32_t D1 = tmem + 64 * (ci & 1);
+            const float gam2 = gamma_of(ci + 2);
             if (!__all_sync(0xffffffffu,
                             mbar_wait_abortable(&full[sg], (ci / kStages) & 1, status, abort_flag)))
                 break;
             // the previous chunk's output is read while MMA1 runs
-            if (warp >= 2 && ci > 0) emit_output(ci - 1);
+            if (qd >= 2 && ci > 0) emit_output(ci - 1);
             if (!__all_sync(0xffffffffu, mbar_wait_abortable(&bar_m1, ci & 1, status, abort_flag)))
                 break;
             tc_fence_after();
-            if (warp < 2) {
-                // ep1: V_new[i] = U[i] - (W S)[i], token i = TMEM lane = d
-                float ws[64];
-                tmem_ld32(tmem_addr(D1, warp, 0), *reinterpret_cast<float(*)[32]>(ws));
-                tmem_ld32(tmem_addr(D1, warp, 32), *reinterpret_cast<float(*)[32]>(ws + 32));
-                const uint32_t stb_off = (uint32_t)sg * kStageBytes;
-                uint4 ur[8];
+            if (qd < 2) {
+                // ep1: V_new[i] = U[i] - (W S)[i], token i = TMEM lane = d, 32 columns
+                float ws[32];
+                tmem_ld32(tmem_addr(D1, qd, 32 * half), ws);
+                const uint32_t ub = (uint32_t)sg * kStage + UO;
+                uint4 ur[4];
 #pragma unroll
-                for (int qd = 0; qd < 8; ++qd) ur[qd] = lds128(sm, stb_off + M::U + sw128_chunk(d, qd));
+                for (int q4 = 0; q4 < 4; ++q4) ur[q4] = lds128(sm, ub + sw128_chunk(d, 4 * half + q4));
 #pragma unroll
-                for (int qd = 0; qd < 8; ++qd) {
+                for (int q4 = 0; q4 < 4; ++q4) {
                     float uf[8], vn[8];
-                    unpack8(ur[qd], uf);
+                    unpack8(ur[q4], uf);
 #pragma unroll
-                    for (int m = 0; m < 8; ++m) vn[m] = uf[m] - ws[qd * 8 + m];
-                    sts128(sm, M::VN + sw128_chunk(d, qd), pack8(vn));
+                    for (int m = 0; m < 8; ++m) vn[m] = uf[m] - ws[q4 * 8 + m];
+                    sts128(sm, M::VN + sw128_chunk(d, 4 * half + q4), pack8(vn));
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
-                named_bar_arrive(kBarVnew, 96);
+                named_bar_arrive(kBarVnew, kVnewCount);
             }
             if (!__all_sync(0xffffffffu, mbar_wait_abortable(&bar_m3, ci & 1, status, abort_flag)))
                 break;
             tc_fence_after();
             {
-                const float gam = reinterpret_cast<const float*>(st + M::GAM)[d];
                 float upd[32];
-                tmem_ld32(tmem_addr(D3, warp, 0), upd);
+                tmem_ld32(tmem_addr(D3, qd, 32 * half), upd);
 #pragma unroll
-                for (int x = 0; x < 32; ++x) S[x] = fmaf(gam, S[x], upd[x]);
-                tmem_ld32(tmem_addr(D3, warp, 32), upd);
-#pragma unroll
-                for (int x = 0; x < 32; ++x) S[32 + x] = fmaf(gam, S[32 + x], upd[x]);
+                for (int x = 0; x < 32; ++x) S[x] = fmaf(gam0, S[x], upd[x]);
             }
             write_state();  // S_{ci+1}; releases the issuer for the next chunk
+            gam0 = gam1;
+            gam1 = gam2;
         }
         // after an expired wait, release the issuer from whichever named barrier it may
         // be waiting at (surplus arrivals are harmless: the CTA ends)
         if (__any_sync(0xffffffffu, *abort_flag != 0)) {
-            named_bar_arrive(kBarState, 160);
-            if (warp < 2) named_bar_arrive(kBarVnew, 96);
+            named_bar_arrive(kBarState, kHoThreads);
+            if (qd < 2) named_bar_arrive(kBarVnew, kVnewCount);
         }
-        if (warp >= 2 && nch > 0 && !*abort_flag) emit_output(nch - 1);
-        if (sN && !*abort_flag) {
-            float4* dst = reinterpret_cast<float4*>(sN + st_off + (size_t)d * 128);
+        if (qd >= 2 && nch > 0 && !*abort_flag) emit_output(nch - 1);
+        if (s_out && !*abort_flag) {
+            float4* dst = reinterpret_cast<float4*>(s_out + st_off);
 #pragma unroll
-            for (int x = 0; x < kVT / 4; ++x)
+            for (int x = 0; x < 8; ++x)
                 dst[x] = make_float4(S[4 * x], S[4 * x + 1], S[4 * x + 2], S[4 * x + 3]);
         }
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+}  // namespace
+
+namespace {
+
+// Second stream and events of the pipelined schedule, one set per device, created on
+// first use and kept for the life of the process (no device memory is allocated).  The
+// mutex keeps two host threads from interleaving their use of the shared events.
+struct PipeRes {
+    bool ready = false;
+    cudaStream_t side = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr, intra_done[3] = {}, ho_done[3] = {};
+};
+PipeRes g_pipe[64];
+std::mutex g_pipe_mu;
+
+cudaError_t pipe_res(int dev, PipeRes** out) {
+    PipeRes& r = g_pipe[dev];
+    if (!r.ready) {
+        int lo = 0, hi = 0;
+        if (cudaError_t e = cudaDeviceGetStreamPriorityRange(&lo, &hi)) return e;
+        // the recurrence (the ordered chain) gets the higher priority
+        if (cudaError_t e = cudaStreamCreateWithPriority(&r.side, cudaStreamNonBlocking, hi))
+            return e;
+        cudaEvent_t* evs[] = {&r.fork, &r.join, &r.intra_done[0], &r.intra_done[1],
+                              &r.intra_done[2], &r.ho_done[0], &r.ho_done[1], &r.ho_done[2]};
+        for (cudaEvent_t* e : evs)
+            if (cudaError_t err = cudaEventCreateWithFlags(e, cudaEventDisableTiming)) return err;
+        r.ready = true;
+    }
+    *out = &r;
+    return cudaSuccess;
 }
 
 }  // namespace
@@ -856,9 +971,9 @@ cudaError_t launch_tc(const void* q, const void* k, const void* v, const float* 
     const int2* stab = reinterpret_cast<const int2*>(ws + L.seq_tab_off);
     const int* count = reinterpret_cast<const int*>(ws + L.count_off);
     int* status = reinterpret_cast<int*>(ws + L.status_off);
+    CUtensorMap tq, tk, tv, tg;
     if (L.max_chunks > 0) {
         const uint64_t rows = (uint64_t)B * T, inner = (uint64_t)H * 128;
-        CUtensorMap tq, tk, tv, tg;
         if (!make_tmap_2d(&tq, q, true, inner, rows, inner * 2, 64, 32, true) ||
             !make_tmap_2d(&tk, k, true, inner, rows, inner * 2, 64, 64, true) ||
             !make_tmap_2d(&tv, v, true, inner, rows, inner * 2, 64, 64, true) ||
@@ -866,21 +981,63 @@ cudaError_t launch_tc(const void* q, const void* k, const void* v, const float* 
             return cudaErrorInvalidValue;
         cudaFuncSetAttribute(kda_intra_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kIntraSmem);
-        const unsigned blocks = (unsigned)(L.max_chunks * H);
-        kda_intra_tc<<<blocks, kIntraThreads, kIntraSmem, s>>>(tq, tk, tv, tg, beta, scale, H, ctab,
-                                                               count, L.max_chunks, records, status);
-        if (cudaError_t e = cudaGetLastError()) return e;
     }
-    if (!record_event(ev, 0, s)) return cudaErrorInvalidResourceHandle;
-    if (L.N > 0) {
-        cudaFuncSetAttribute(kda_h_o_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kHoSmem);
-        const unsigned blocks = (unsigned)L.N * H * 2;
-        kda_h_o_tc<<<blocks, kHoThreads, kHoSmem, s>>>(records, ctab, stab, L.max_chunks, s0,
-                                                       static_cast<__nv_bfloat16*>(o), sN, H, status);
-        if (cudaError_t e = cudaGetLastError()) return e;
+    cudaFuncSetAttribute(kda_h_o_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kHoSmem);
+    __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(o);
+    const unsigned ho_blocks = (unsigned)L.N * H * 2;
+
+    // Whole-problem schedule: one launch of each kernel (and the only one with per-kernel
+    // timing events).
+    if (L.span == 0 || ev) {
+        if (L.max_chunks > 0) {
+            const unsigned blocks = (unsigned)(L.max_chunks * H);
+            kda_intra_tc<<<blocks, kIntraThreads, kIntraSmem, s>>>(
+                tq, tk, tv, tg, beta, scale, H, ctab, stab, count, L.max_chunks, RangeArgs{},
+                records, status);
+            if (cudaError_t e = cudaGetLastError()) return e;
+        }
+        if (!record_event(ev, 0, s)) return cudaErrorInvalidResourceHandle;
+        if (L.N > 0) {
+            kda_h_o_tc<<<ho_blocks, kHoThreads, kHoSmem, s>>>(records, ctab, stab, L.max_chunks,
+                                                              RangeArgs{}, s0, ob, sN, H, status);
+            if (cudaError_t e = cudaGetLastError()) return e;
+        }
+        if (!record_event(ev, 1, s)) return cudaErrorInvalidResourceHandle;
+        return cudaSuccess;
     }
-    if (!record_event(ev, 1, s)) return cudaErrorInvalidResourceHandle;
-    return cudaSuccess;
+
+    // Pipelined schedule: range r's intra-chunk kernel on the caller's stream, its
+    // recurrence on the side stream once range r's records exist and range r - 1's
+    // recurrence has handed over the state; records live in a ring of L.ring range slots,
+    // so intra of range r waits for the recurrence of range r - ring to have read them.
+    int dev = 0;
+    if (cudaError_t e = cudaGetDevice(&dev)) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_pipe_mu);
+    PipeRes* P = nullptr;
+    if (cudaError_t e = pipe_res(dev, &P)) return e;
+    float* carry = reinterpret_cast<float*>(ws + L.carry_off);
+    const size_t slot_bytes = (size_t)L.N * L.span * H * TcRecord::bytes;
+    if (cudaError_t e = cudaEventRecord(P->fork, s)) return e;
+    if (cudaError_t e = cudaStreamWaitEvent(P->side, P->fork, 0)) return e;
+    for (int r = 0; r < L.ranges; ++r) {
+        const int sl = r % L.ring;
+        uint8_t* rec = records + sl * slot_bytes;
+        const RangeArgs ra{r * L.span, L.span, carry};
+        if (r >= L.ring)
+            if (cudaError_t e = cudaStreamWaitEvent(s, P->ho_done[sl], 0)) return e;
+        kda_intra_tc<<<(unsigned)(L.N * L.span * H), kIntraThreads, kIntraSmem, s>>>(
+            tq, tk, tv, tg, beta, scale, H, ctab, stab, count, L.max_chunks, ra, rec, status);
+        if (cudaError_t e = cudaGetLastError()) return e;
+        if (cudaError_t e = cudaEventRecord(P->intra_done[sl], s)) return e;
+        if (cudaError_t e = cudaStreamWaitEvent(P->side, P->intra_done[sl], 0)) return e;
+        kda_h_o_tc<<<ho_blocks, kHoThreads, kHoSmem, P->side>>>(rec, ctab, stab, L.max_chunks, ra,
+                                                                 s0, ob, sN, H, status);
+        if (cudaError_t e = cudaGetLastError()) return e;
+        if (cudaError_t e = cudaEventRecord(P->ho_done[sl], P->side)) return e;
+    }
+    if (cudaError_t e = cudaEventRecord(P->join, P->side)) return e;
+    return cudaStreamWaitEvent(s, P->join, 0);
 }
 
 }  // namespace kda

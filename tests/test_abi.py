@@ -38,7 +38,24 @@ def test_status_strings(lib):
     for s in range(8):
         assert lib.kda_status_string(s).decode()
     assert lib.kda_status_string(99).decode() == "unknown status"
-    assert lib.kda_abi_version() == 100
+    assert lib.kda_abi_version() == 101
+
+
+def test_launch_count(lib):
+    """Whole-problem schedule: 3 launches; pipelined (bf16 K = V = 128, fixed length,
+    <= 128 chains, >= 512 chunks per sequence): chunk index + 2 per range of 32 chunks."""
+    lc = lambda *a: lib.kda_fwd_launch_count(*a)
+    bf16, f32 = 0, 1
+    assert lc(2, 4096, 16, 128, 128, 0, 64, bf16) == 3             # 64 chunks
+    assert lc(1, 131072, 32, 128, 128, 0, 64, bf16) == 1 + 2 * 64  # 2048 chunks
+    assert lc(1, 512 * 64, 2, 128, 128, 0, 64, bf16) == 1 + 2 * 16
+    assert lc(1, 511 * 64, 2, 128, 128, 0, 64, bf16) == 3          # 511 chunks
+    assert lc(1, 600 * 64 + 5, 2, 128, 128, 0, 64, bf16) == 1 + 2 * 19
+    assert lc(32, 2048, 32, 128, 128, 0, 64, bf16) == 3            # 1024 chains
+    assert lc(1, 37000, 32, 128, 128, 8, 64, bf16) == 3            # packed
+    assert lc(1, 131072, 32, 128, 128, 0, 64, f32) == 3            # fp32 path
+    assert lc(1, 131072, 32, 64, 64, 0, 64, bf16) == 3             # other shapes
+    assert lc(2, 4096, 16, 128, 128, 0, 32, bf16) == -1            # rejected sizes
 
 
 def test_workspace_bytes_rules(lib):

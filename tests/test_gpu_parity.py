@@ -138,6 +138,26 @@ def test_deterministic(kda):
         assert torch.equal(o0, o1) and torch.equal(f0, f1)
 
 
+@pytest.mark.parametrize("shape", [(1, 64 * 512, 2, 0.1), (2, 64 * 600 + 37, 1, None)],
+                         ids=["512chunks_init", "601chunks_tail"])
+def test_pipelined_schedule(kda, orc, shape):
+    """The pipelined schedule (chunk ranges on two streams, state handed over in fp32)
+    gives bit-identical results to the whole-problem schedule, and matches the oracle."""
+    B, T, H, init = shape
+    inp = make_inputs(custom(B=B, T=T, H=H, K=128, V=128, dtype=torch.bfloat16,
+                             init_std=init, seed=T + H), device="cuda")
+    assert kda.launch_count(B, T, H, 128, 128) > 3   # really pipelined
+    o_p, f_p = run_gpu(kda, inp)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    for e in evs:
+        e.record()
+    o_w, f_w = run_gpu(kda, inp, events=evs)         # whole-problem schedule
+    assert torch.equal(o_p, o_w) and torch.equal(f_p, f_w)
+    o_ref, f_ref = run_oracle(orc, inp)
+    eo, ef = errors(o_p, f_p, o_ref, f_ref)
+    assert eo <= 2e-2 and ef <= 2e-2, (eo, ef)
+
+
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
 def test_split_call_resume(kda, dtype):
     inp = make_inputs(custom(B=2, T=300, H=2, K=128, V=128, dtype=dtype, init_std=0.1, seed=43),
