@@ -31,7 +31,7 @@ sys.path.insert(0, ROOT)
 
 import torch  # noqa: E402
 
-from workloads import WORKLOADS, make_inputs  # noqa: E402
+from workloads import DECODE_WORKLOADS, WORKLOADS, make_decode_inputs, make_inputs  # noqa: E402
 
 METRIC = "KDA fwd tokens/s and TFLOP/s (bf16, H=16, K=V=128, T=4096); % of roofline"
 UNIT = "tokens/s"
@@ -409,19 +409,96 @@ def run_ours(args, rank, world, local):
     return 0
 
 
+# ---------------------------------------------------------------------------
+# decode step (a second workload on the same state)
+# ---------------------------------------------------------------------------
+
+def run_decode(args, rank, world, local):
+    """Times kda_decode: one token for each of N sequences; HBM-bound on the state."""
+    import kimi_delta_attention_11_gb300 as kda
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    kda.load_library()
+    spec = DECODE_WORKLOADS[args.workload]
+    inp = make_decode_inputs(device=str(dev), **spec)
+    N, H, K, V, dt = (inp[x] for x in ("N", "H", "K", "V", "dtype"))
+    esz = 2 if dt == torch.bfloat16 else 4
+    state_bytes = N * H * K * V * 4
+    step_bytes = 2 * state_bytes + N * H * (esz * (2 * K + 2 * V) + 4 * K + 4)
+    o = torch.empty((N, H, V), dtype=dt, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(4 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        kda.decode(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["state"],
+                   inp["scale"], out=o)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        ev_a[i].record(stream)
+        step()
+        ev_b[i].record(stream)
+    barrier(world)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in zip(ev_a, ev_b)) / args.steps, world, dev)
+    clocks = sampler.stop()
+    assert torch.isfinite(o.float()).all().item() and torch.isfinite(inp["state"]).all().item()
+    if rank != 0:
+        return 0
+    peak, peak_kind = measured_peaks()
+    achieved = step_bytes / (ms * 1e-3) / 1e9
+    line = {
+        "metric": "KDA decode step tokens/s (one token per sequence)", "value": N * world / (ms * 1e-3),
+        "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if dt == torch.bfloat16 else "f32", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: N={N} H={H} K={K} V={V}",
+                   "l2": "flushed between timed steps (write of 4x L2)"},
+        "roofline": {"bound": "hbm", "kernel": "kda_decode_kernel", "achieved": achieved,
+                     "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": f"{peak_kind} hbm_gbs", "traffic": None,
+                     "bytes_per_step": step_bytes},
+        "gpu_launches": args.steps, "clocks": clocks, "wall_s_timed": wall,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[1])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="dense_bf16")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + sorted(DECODE_WORKLOADS),
+                    default="dense_bf16")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank, world, local = dist_info()
+    if args.workload in DECODE_WORKLOADS:
+        if args.impl == "reference":
+            ap.error("the decode workload has no reference arm")
+        init_dist(world)
+        try:
+            return run_decode(args, rank, world, local)
+        finally:
+            if world > 1 and torch.distributed.is_initialized():
+                torch.distributed.destroy_process_group()
     if args.impl == "reference":
         return run_reference(args, rank, world)
     init_dist(world)

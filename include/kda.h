@@ -62,6 +62,29 @@ typedef enum kda_dtype {
     KDA_DTYPE_F32 = 1
 } kda_dtype;
 
+/* Gate activation and q/k normalisation performed inside the kernels (Tokamax design
+ * doc 9.1.3, use_gate_in_kernel; "KDAChunkwise", FP32 core, F.normalize).  Pass NULL
+ * (or a zeroed struct) for the plain behaviour: g holds ln(alpha) and q, k are used as
+ * given.
+ *   use_gate_in_kernel  non-zero: g holds the raw gate x, and with
+ *                       lambda_h = exp(a_log[h]) and x' = x + dt_bias[h*K + d]:
+ *                         lower_bound == 0:  ln(alpha) = -lambda_h * softplus(x')
+ *                         -5 <= lower_bound < 0:  ln(alpha) = lower_bound * sigmoid(lambda_h x')
+ *                       (any other lower_bound is KDA_ERR_INVALID_ARG).
+ *   a_log               fp32 device [H]; required when use_gate_in_kernel.
+ *   dt_bias             nullable fp32 device [H*K].
+ *   qk_l2norm           non-zero: q and k are divided by max(||.||_2, 1e-6) along K
+ *                       (in fp32) before use.
+ * Rows past the end of a sequence are identity steps whatever the raw gate holds, so no
+ * -1e4 padding of raw gates (Tokamax design doc 9.1.7) is needed. */
+typedef struct kda_gate_options {
+    int use_gate_in_kernel;
+    const float* a_log;
+    const float* dt_bias;
+    float lower_bound;
+    int qk_l2norm;
+} kda_gate_options;
+
 /* Bytes of device workspace kda_fwd needs for these sizes (0 on invalid sizes).
  * Packed input (num_seqs > 0 together with a non-null cu_seqlens at call time) needs
  * room for ceil(T/64) + num_seqs - 1 chunks per head; fixed length for B * ceil(T/64).
@@ -115,13 +138,39 @@ kda_status kda_fwd(const void* q, const void* k, const void* v, const float* g,
                    void* o, float* final_state, int B, int T, int H, int K, int V,
                    kda_dtype dtype, void* workspace, size_t workspace_bytes, void* stream);
 
+/* kda_fwd with gate activation / q-k normalisation options (`opts` nullable: then this
+ * is kda_fwd).  Same arguments, layouts and rules otherwise. */
+kda_status kda_fwd_ex(const void* q, const void* k, const void* v, const float* g,
+                      const float* beta, float scale, int chunk_size,
+                      const float* initial_state, const int32_t* cu_seqlens, int num_seqs,
+                      void* o, float* final_state, int B, int T, int H, int K, int V,
+                      kda_dtype dtype, void* workspace, size_t workspace_bytes,
+                      const kda_gate_options* opts, void* stream);
+
+/* One decode step: every one of N sequences advances by one token, in the recurrent form
+ * (Tokamax design doc 9.1.2, Eq. (1) in delta-correction form; "KDA Doesn't Care About
+ * the Future", "Chunkwise KDA in Broad Strokes": the recurrence decodes a token at a time):
+ *   S <- Diag(exp g) S;  e = v - S^T k;  S <- S + beta k e^T;  o = scale S^T q.
+ *   q, k     [N,H,K] of `dtype`;  v, o [N,H,V] of `dtype` (o written);
+ *   g        fp32 [N,H,K] (ln(alpha), or the raw gate with opts->use_gate_in_kernel);
+ *   beta     fp32 [N,H];  state  fp32 [N,H,K,V], read and updated in place (required);
+ *   opts     nullable, as for kda_fwd_ex.
+ * K, V in {64, 128}; pointers aligned to their element size; N == 0 is a no-op.  No
+ * workspace, no allocation, asynchronous on `stream`. */
+kda_status kda_decode(const void* q, const void* k, const void* v, const float* g,
+                      const float* beta, float scale, float* state, void* o, int N, int H,
+                      int K, int V, kda_dtype dtype, const kda_gate_options* opts,
+                      void* stream);
+
 /* kda_fwd, plus CUDA events recorded on `stream` around its stages, for timing each
  * kernel on the stream it runs on.  `events` holds num_events cudaEvent_t handles
  * created by the caller; events[0] is recorded before the first launch and events[i]
  * after stage i, for the stages in order: 1 chunk index, 2 intra-chunk kernel,
  * 3 recurrence/output kernel.  num_events must be 0 (then this is kda_fwd) or at
  * least 4 (KDA_ERR_INVALID_ARG otherwise).  A stage with nothing to do (T == 0)
- * still gets its event recorded.  With events the kernels always run back to back on
+ * still gets its event recorded (fixed-length bf16 input with K = V = 128 has no
+ * chunk-index kernel: its chunk positions are arithmetic).  With events the kernels
+ * always run back to back on
  * `stream`, one launch each over the whole problem (never the pipelined schedule), so
  * that each stage is one kernel's time; results are identical. */
 kda_status kda_fwd_profiled(const void* q, const void* k, const void* v, const float* g,
@@ -191,13 +240,15 @@ kda_status kda_get_device_status(const void* workspace, void* stream);
  * Used by the tests to check the building blocks in isolation; not part of the
  * forward pass.  Modes 2 and 3 check the MN-major operand form: in mode 2 B is given as
  * its transpose [K][N] (N >= 64), in mode 3 A is given as its transpose [K][128]; the
- * result is the same product. */
+ * result is the same product.  Mode 4 keeps A in tensor memory (written with
+ * tcgen05.st) and B in shared memory. */
 kda_status kda_selftest_umma(const void* A, const void* B, float* D, int N, int K, int mode,
                              int* status, void* stream);
 
-/* Number of kernel launches kda_fwd makes for these sizes (chunk index, intra-chunk and
- * recurrence kernels; pipelined calls launch the last two once per chunk range), or -1
- * for sizes kda_fwd rejects. */
+/* Number of kernel launches kda_fwd makes for these sizes: the chunk-index kernel
+ * (packed input, and the fp32 / other-shape path), the intra-chunk kernel and the
+ * recurrence kernel (pipelined calls launch the last two once per chunk range); -1 for
+ * sizes kda_fwd rejects. */
 int kda_fwd_launch_count(int B, int T, int H, int K, int V, int num_seqs, int chunk_size,
                          kda_dtype dtype);
 

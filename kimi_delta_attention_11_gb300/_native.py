@@ -37,6 +37,13 @@ class KdaError(RuntimeError):
 _LIB = None
 _LOCK = threading.Lock()
 
+
+class _GateOptions(ctypes.Structure):
+    """kda_gate_options of include/kda.h."""
+    _fields_ = [("use_gate_in_kernel", ctypes.c_int), ("a_log", ctypes.c_void_p),
+                ("dt_bias", ctypes.c_void_p), ("lower_bound", ctypes.c_float),
+                ("qk_l2norm", ctypes.c_int)]
+
 _vp, _sz, _i, _f = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_float
 _SIGNATURES = {
     "kda_fwd_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i, _i, _i]),
@@ -47,6 +54,10 @@ _SIGNATURES = {
                               ctypes.POINTER(ctypes.c_void_p), _i]),
     "kda_fwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _f, _i, _vp, _vp, _i, _vp, _vp,
                              _i, _i, _i, _i, _i, _i, _vp]),
+    "kda_fwd_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _f, _i, _vp, _vp, _i, _vp, _vp,
+                        _i, _i, _i, _i, _i, _i, _vp, _sz, ctypes.POINTER(_GateOptions), _vp]),
+    "kda_decode": (_i, [_vp, _vp, _vp, _vp, _vp, _f, _vp, _vp, _i, _i, _i, _i, _i,
+                        ctypes.POINTER(_GateOptions), _vp]),
     "kda_build_chunk_index": (_i, [_vp, _i, _i, _i, _i, _vp, _sz, ctypes.POINTER(_sz),
                                    ctypes.POINTER(_sz), ctypes.POINTER(_sz), _vp]),
     "kda_selftest_umma": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp, _vp]),
@@ -115,13 +126,31 @@ def launch_count(B: int, T: int, H: int, K: int, V: int, num_seqs: int = 0,
     return int(n)
 
 
+def _gate_struct(gate: Optional[dict], H: int, K: int):
+    """Validated kda_gate_options from a dict with keys a_log ([H] fp32 CUDA),
+    dt_bias (optional [H*K] fp32 CUDA), lower_bound (float, 0 = softplus form),
+    use_gate_in_kernel (default True when a_log is given) and qk_l2norm (bool)."""
+    if gate is None:
+        return None
+    a_log, dt_bias = gate.get("a_log"), gate.get("dt_bias")
+    use = bool(gate.get("use_gate_in_kernel", a_log is not None))
+    for name, t, n in (("a_log", a_log, H), ("dt_bias", dt_bias, H * K)):
+        if t is not None and (not t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous()
+                              or t.numel() != n):
+            raise ValueError(f"{name} must be a contiguous fp32 CUDA tensor of {n} elements")
+    opts = _GateOptions(int(use), None if a_log is None else a_log.data_ptr(),
+                        None if dt_bias is None else dt_bias.data_ptr(),
+                        float(gate.get("lower_bound", 0.0)), int(bool(gate.get("qk_l2norm", False))))
+    return opts
+
+
 def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
         beta: torch.Tensor, scale: Optional[float] = None,
         initial_state: Optional[torch.Tensor] = None,
         cu_seqlens: Optional[torch.Tensor] = None, output_final_state: bool = True,
         chunk_size: int = 64, workspace: Optional[torch.Tensor] = None,
         out: Optional[torch.Tensor] = None, final_state: Optional[torch.Tensor] = None,
-        events=None):
+        events=None, gate: Optional[dict] = None):
     """Chunkwise KDA forward on the current CUDA stream (no host synchronisation).
 
     q, k: [B,T,H,K]; v: [B,T,H,V] (bf16 or fp32, all the same dtype); g: [B,T,H,K] fp32;
@@ -131,6 +160,9 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
     ``events``: optional list of >= 4 ``torch.cuda.Event`` recorded around the stages
     (chunk index, intra-chunk kernel, recurrence kernel) for per-kernel timing; with
     events the kernels run back to back, one launch each (see include/kda.h).
+    ``gate``: optional in-kernel gate activation / q-k normalisation (kda_fwd_ex):
+    dict(a_log=[H] fp32, dt_bias=[H*K] fp32 or None, lower_bound=0.0 (softplus form) or
+    in [-5, 0) (sigmoid form), qk_l2norm=bool); g then holds raw gates when a_log is set.
     """
     lib = load_library()
     B, T, H, K = q.shape
@@ -165,7 +197,12 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
             _ptr(initial_state), _ptr(cu_seqlens), num_seqs, _ptr(o), _ptr(fin),
             B, T, H, K, V, DTYPE_CODES[q.dtype], _ptr(workspace),
             workspace.numel() * workspace.element_size(), _stream_handle(dev))
-    if events is None:
+    opts = _gate_struct(gate, H, K)
+    if opts is not None:
+        if events is not None:
+            raise ValueError("events and gate options cannot be combined")
+        st = lib.kda_fwd_ex(*args[:-1], ctypes.byref(opts), args[-1])
+    elif events is None:
         st = lib.kda_fwd(*args)
     else:
         if any(e.cuda_event == 0 for e in events):
@@ -175,6 +212,36 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
     if st != KDA_OK:
         raise KdaError(st, "kda_fwd")
     return o, fin
+
+
+def decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+           beta: torch.Tensor, state: torch.Tensor, scale: Optional[float] = None,
+           out: Optional[torch.Tensor] = None, gate: Optional[dict] = None) -> torch.Tensor:
+    """One decode step on the current CUDA stream: q, k [N,H,K], v [N,H,V] (bf16 or fp32),
+    g [N,H,K] fp32, beta [N,H] fp32, state [N,H,K,V] fp32 updated in place.  Returns o
+    [N,H,V] in q.dtype.  ``gate`` as for fwd."""
+    lib = load_library()
+    N, H, K = q.shape
+    V = v.shape[-1]
+    if scale is None:
+        scale = K ** -0.5
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("state", state)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if k.dtype != q.dtype or v.dtype != q.dtype or q.dtype not in DTYPE_CODES:
+        raise ValueError("q, k, v must share one dtype, bf16 or fp32")
+    if g.dtype != torch.float32 or beta.dtype != torch.float32 or state.dtype != torch.float32:
+        raise ValueError("g, beta and state must be fp32")
+    if tuple(state.shape) != (N, H, K, V):
+        raise ValueError("state must be [N, H, K, V]")
+    o = out if out is not None else torch.empty((N, H, V), dtype=q.dtype, device=q.device)
+    opts = _gate_struct(gate, H, K)
+    st = lib.kda_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+                        _ptr(state), _ptr(o), N, H, K, V, DTYPE_CODES[q.dtype],
+                        None if opts is None else ctypes.byref(opts), _stream_handle(q.device))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_decode")
+    return o
 
 
 def build_chunk_index(cu_seqlens: Optional[torch.Tensor], B: int, T: int,

@@ -23,6 +23,7 @@ Layout make_layout(int B, int T, int H, int K, int V, int num_seqs, bool packed,
     L.inter_stride = use_tc_path(K, V, dt) ? (size_t)TcRecord::bytes
                                            : align_up(SimtRecord::floats(K, V) * sizeof(float), 1024);
     L.total = L.inter_off + (size_t)L.max_chunks * H * L.inter_stride;
+    L.fixed = use_tc_path(K, V, dt) && !packed;
     // Pipelining pays when the recurrence has few, long chains (its ordered chunk steps,
     // not the SM count, set its time): fixed-length input, at most 128 (sequence, head)
     // chains and at least 512 chunks per sequence (measured on GB300: a 6 % gain at
@@ -97,8 +98,9 @@ int kda_fwd_launch_count(int B, int T, int H, int K, int V, int num_seqs, int ch
     const bool packed = num_seqs > 0;
     if (check_sizes(B, T, H, K, V, num_seqs, packed, chunk_size, dtype) != KDA_OK) return -1;
     const Layout L = make_layout(B, T, H, K, V, num_seqs, packed, dtype);
-    if (use_tc_path(K, V, dtype) && L.span > 0) return 1 + 2 * L.ranges;
-    return 1 + (L.max_chunks > 0 ? 1 : 0) + (L.N > 0 ? 1 : 0);
+    const int index = L.fixed ? 0 : 1;
+    if (L.span > 0) return index + 2 * L.ranges;
+    return index + (L.max_chunks > 0 ? 1 : 0) + (L.N > 0 ? 1 : 0);
 }
 
 const char* kda_status_string(int status) {
@@ -146,15 +148,41 @@ kda_status kda_build_chunk_index(const int32_t* cu_seqlens, int num_seqs, int B,
     return KDA_OK;
 }
 
-kda_status kda_fwd_profiled(const void* q, const void* k, const void* v, const float* g,
-                            const float* beta, float scale, int chunk_size,
-                            const float* initial_state, const int32_t* cu_seqlens, int num_seqs,
-                            void* o, float* final_state, int B, int T, int H, int K, int V,
-                            kda_dtype dtype, void* workspace, size_t workspace_bytes,
-                            void* stream, void* const* events, int num_events) {
+}  // extern "C"
+
+namespace {
+
+// kda_gate_options -> the kernels' GateArgs; KDA_OK or the validation failure.
+kda_status gate_args(const kda_gate_options* opts, GateArgs* ga) {
+    *ga = GateArgs{};
+    if (!opts) return KDA_OK;
+    if (opts->use_gate_in_kernel) {
+        if (!opts->a_log) return KDA_ERR_INVALID_ARG;
+        if (!aligned4(opts->a_log) || (opts->dt_bias && !aligned4(opts->dt_bias)))
+            return KDA_ERR_ALIGNMENT;
+        const float lb = opts->lower_bound;
+        // Tokamax design doc 5.3: a lower bound selects the sigmoid form, -5 <= lb < 0
+        if (lb != 0.f && !(lb >= -5.f && lb < 0.f)) return KDA_ERR_INVALID_ARG;
+        ga->mode = lb == 0.f ? 1 : 2;
+        ga->a_log = opts->a_log;
+        ga->dt_bias = opts->dt_bias;
+        ga->lower_bound = lb;
+    }
+    ga->qk_l2norm = opts->qk_l2norm ? 1 : 0;
+    return KDA_OK;
+}
+
+kda_status fwd_impl(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                    float scale, int chunk_size, const float* initial_state,
+                    const int32_t* cu_seqlens, int num_seqs, void* o, float* final_state, int B,
+                    int T, int H, int K, int V, kda_dtype dtype, void* workspace,
+                    size_t workspace_bytes, const kda_gate_options* opts, void* stream,
+                    void* const* events, int num_events) {
     const bool packed = cu_seqlens != nullptr;
     if (kda_status st = check_sizes(B, T, H, K, V, num_seqs, packed, chunk_size, dtype))
         return st;
+    GateArgs ga;
+    if (kda_status st = gate_args(opts, &ga)) return st;
     // With T == 0 no token tensor is read or written, so its pointers may be anything.
     const bool tokens = T > 0;
     if (tokens && (!q || !k || !v || !g || !beta || !o)) return KDA_ERR_INVALID_ARG;
@@ -177,16 +205,32 @@ kda_status kda_fwd_profiled(const void* q, const void* k, const void* v, const f
     };
     if (!mark(0)) return KDA_ERR_CUDA;
     if (cudaMemsetAsync(ws, 0, 256, s) != cudaSuccess) return KDA_ERR_CUDA;
-    if (launch_chunk_index(cu_seqlens, L.N, T, L, ws, s) != cudaSuccess) return KDA_ERR_CUDA;
+    if (!L.fixed && launch_chunk_index(cu_seqlens, L.N, T, L, ws, s) != cudaSuccess)
+        return KDA_ERR_CUDA;
     if (!mark(1)) return KDA_ERR_CUDA;
     const cudaError_t e =
         use_tc_path(K, V, dtype)
-            ? launch_tc(q, k, v, g, beta, scale, initial_state, o, final_state, B, T, H, L, ws, s,
-                        num_events ? events + 2 : nullptr)
-            : launch_simt(q, k, v, g, beta, scale, initial_state, o, final_state, H, K, V, dtype,
-                          L, ws, s, num_events ? events + 2 : nullptr);
+            ? launch_tc(q, k, v, g, beta, scale, ga, initial_state, o, final_state, B, T, H, L,
+                        ws, s, num_events ? events + 2 : nullptr)
+            : launch_simt(q, k, v, g, beta, scale, ga, initial_state, o, final_state, H, K, V,
+                          dtype, L, ws, s, num_events ? events + 2 : nullptr);
     if (e != cudaSuccess) return KDA_ERR_CUDA;
     return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kda_status kda_fwd_profiled(const void* q, const void* k, const void* v, const float* g,
+                            const float* beta, float scale, int chunk_size,
+                            const float* initial_state, const int32_t* cu_seqlens, int num_seqs,
+                            void* o, float* final_state, int B, int T, int H, int K, int V,
+                            kda_dtype dtype, void* workspace, size_t workspace_bytes,
+                            void* stream, void* const* events, int num_events) {
+    return fwd_impl(q, k, v, g, beta, scale, chunk_size, initial_state, cu_seqlens, num_seqs, o,
+                    final_state, B, T, H, K, V, dtype, workspace, workspace_bytes, nullptr, stream,
+                    events, num_events);
 }
 
 kda_status kda_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
@@ -194,9 +238,43 @@ kda_status kda_fwd(const void* q, const void* k, const void* v, const float* g, 
                    const int32_t* cu_seqlens, int num_seqs, void* o, float* final_state, int B,
                    int T, int H, int K, int V, kda_dtype dtype, void* workspace,
                    size_t workspace_bytes, void* stream) {
-    return kda_fwd_profiled(q, k, v, g, beta, scale, chunk_size, initial_state, cu_seqlens,
-                            num_seqs, o, final_state, B, T, H, K, V, dtype, workspace,
-                            workspace_bytes, stream, nullptr, 0);
+    return fwd_impl(q, k, v, g, beta, scale, chunk_size, initial_state, cu_seqlens, num_seqs, o,
+                    final_state, B, T, H, K, V, dtype, workspace, workspace_bytes, nullptr, stream,
+                    nullptr, 0);
+}
+
+kda_status kda_fwd_ex(const void* q, const void* k, const void* v, const float* g,
+                      const float* beta, float scale, int chunk_size,
+                      const float* initial_state, const int32_t* cu_seqlens, int num_seqs,
+                      void* o, float* final_state, int B, int T, int H, int K, int V,
+                      kda_dtype dtype, void* workspace, size_t workspace_bytes,
+                      const kda_gate_options* opts, void* stream) {
+    return fwd_impl(q, k, v, g, beta, scale, chunk_size, initial_state, cu_seqlens, num_seqs, o,
+                    final_state, B, T, H, K, V, dtype, workspace, workspace_bytes, opts, stream,
+                    nullptr, 0);
+}
+
+kda_status kda_decode(const void* q, const void* k, const void* v, const float* g,
+                      const float* beta, float scale, float* state, void* o, int N, int H, int K,
+                      int V, kda_dtype dtype, const kda_gate_options* opts, void* stream) {
+    if (N < 0 || H < 1 || K < 1 || V < 1) return KDA_ERR_INVALID_ARG;
+    if (dtype != KDA_DTYPE_BF16 && dtype != KDA_DTYPE_F32) return KDA_ERR_INVALID_ARG;
+    if (K > 256 || V > 256) return KDA_ERR_INVALID_ARG;
+    if ((K != 64 && K != 128) || (V != 64 && V != 128)) return KDA_ERR_UNSUPPORTED;
+    GateArgs ga;
+    if (kda_status st = gate_args(opts, &ga)) return st;
+    if (N == 0) return KDA_OK;
+    if (!q || !k || !v || !g || !beta || !state || !o) return KDA_ERR_INVALID_ARG;
+    const size_t es = dtype == KDA_DTYPE_BF16 ? 2 : 4;
+    auto al = [](const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; };
+    if (!al(q, es) || !al(k, es) || !al(v, es) || !al(o, es) || !aligned4(g) || !aligned4(beta) ||
+        !aligned4(state))
+        return KDA_ERR_ALIGNMENT;
+    if ((long long)N * H * K * V >= (1ll << 40)) return KDA_ERR_INVALID_ARG;
+    if (kda_status d = check_device()) return d;
+    const cudaError_t e = launch_decode(q, k, v, g, beta, scale, ga, state, o, N, H, K, V, dtype,
+                                        static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
 kda_status kda_get_device_status(const void* workspace, void* stream) {

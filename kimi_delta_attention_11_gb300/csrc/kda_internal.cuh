@@ -36,7 +36,63 @@ struct Layout {
     // of range r + 1 runs on the caller's stream while the recurrence of range r runs on
     // a second stream.  span == 0: one launch of each kernel over the whole problem.
     int span = 0, ranges = 0, ring = 0;
+    // fixed-length input on the tensor-core path: chunk facts are arithmetic (ChunkIndex)
+    // and no chunk-index kernel runs
+    bool fixed = false;
 };
+
+// Where the kernels find a chunk's sequence, first token, length and index within its
+// sequence.  Packed input: the tables the chunk-index kernel builds in the workspace.
+// Fixed-length input (the bf16 tensor-core path): sequence n is tokens [n T, (n + 1) T),
+// so the same facts follow arithmetically and that path launches no index kernel.
+struct ChunkIndex {
+    const int4* chunk_tab = nullptr;  // {sequence, first token, length, index in sequence}
+    const int2* seq_tab = nullptr;    // {first chunk, number of chunks}
+    const int* count = nullptr;       // number of chunks
+    int fixed = 0, T = 0, nct = 0;    // fixed length: T tokens, nct chunks per sequence
+#ifdef __CUDACC__
+    __device__ __forceinline__ int4 chunk(long long c) const {
+        if (!fixed) return chunk_tab[c];
+        const int n = (int)(c / nct), j = (int)(c - (long long)n * nct);
+        return make_int4(n, n * T + j * kChunk, min(kChunk, T - j * kChunk), j);
+    }
+    __device__ __forceinline__ int2 seq(int n) const {
+        return fixed ? make_int2(n * nct, nct) : seq_tab[n];
+    }
+    // number of chunks, given the launch's upper bound (exact for fixed length)
+    __device__ __forceinline__ long long num_chunks(long long max_chunks) const {
+        return fixed ? max_chunks : *count;
+    }
+#endif
+};
+
+// Gate activation and q/k normalisation inside the kernels (Tokamax design doc 9.1.3,
+// use_gate_in_kernel; "KDAChunkwise", FP32 core: F.normalize with eps 1e-6).  mode 0: g
+// holds ln(alpha) as given; mode 1: g is a raw gate, ln(alpha) = -exp(a_log[h]) *
+// softplus(g + dt_bias); mode 2: ln(alpha) = lower_bound * sigmoid(exp(a_log[h]) *
+// (g + dt_bias)).  qk_l2norm: q and k are divided by max(||.||_2, 1e-6) along K first.
+struct GateArgs {
+    int mode = 0;
+    const float* a_log = nullptr;    // [H]
+    const float* dt_bias = nullptr;  // [H * K] or null
+    float lower_bound = 0.f;
+    int qk_l2norm = 0;
+};
+
+#ifdef __CUDACC__
+// ln(alpha) of key channel d of head h from the gate input x as the kernels read it.
+__device__ __forceinline__ float gate_log_decay(const GateArgs& ga, float x, int h, int d, int K) {
+    if (ga.mode == 0) return x;
+    if (ga.dt_bias) x += ga.dt_bias[(size_t)h * K + d];
+    const float lam = expf(ga.a_log[h]);
+    if (ga.mode == 1) {
+        // softplus, with the usual linear branch where exp would overflow the sum
+        const float sp = x > 20.f ? x : log1pf(expf(x));
+        return -lam * sp;
+    }
+    return ga.lower_bound / (1.f + expf(-lam * x));
+}
+#endif
 
 // Chunk range of one kernel launch: chunks j0 <= j < j0 + span of every sequence
 // (j = index within the sequence); span == 0 means all chunks.  carry: the state buffer
@@ -106,13 +162,16 @@ Layout make_layout(int B, int T, int H, int K, int V, int num_seqs, bool packed,
 cudaError_t launch_chunk_index(const int32_t* cu_seqlens, int N, int T, const Layout& L,
                                char* ws, cudaStream_t s);
 cudaError_t launch_tc(const void* q, const void* k, const void* v, const float* g,
-                      const float* beta, float scale, const float* s0, void* o, float* sN, int B,
-                      int T, int H, const Layout& L, char* ws, cudaStream_t s,
+                      const float* beta, float scale, const GateArgs& ga, const float* s0, void* o,
+                      float* sN, int B, int T, int H, const Layout& L, char* ws, cudaStream_t s,
                       void* const* events_after);
+cudaError_t launch_decode(const void* q, const void* k, const void* v, const float* g,
+                          const float* beta, float scale, const GateArgs& ga, float* state,
+                          void* o, int N, int H, int K, int V, kda_dtype dt, cudaStream_t s);
 cudaError_t launch_simt(const void* q, const void* k, const void* v, const float* g,
-                        const float* beta, float scale, const float* s0, void* o, float* sN,
-                        int H, int K, int V, kda_dtype dt, const Layout& L, char* ws,
-                        cudaStream_t s, void* const* events_after);
+                        const float* beta, float scale, const GateArgs& ga, const float* s0,
+                        void* o, float* sN, int H, int K, int V, kda_dtype dt, const Layout& L,
+                        char* ws, cudaStream_t s, void* const* events_after);
 
 // Records events_after[i] (a cudaEvent_t) on s when events_after is non-null.
 inline bool record_event(void* const* events_after, int i, cudaStream_t s) {

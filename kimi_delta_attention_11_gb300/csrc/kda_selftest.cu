@@ -2,6 +2,8 @@
 // building blocks as the bf16 kernels: D[128][N] = A[128][K] * B[N][K]^T.
 // Mode 0 stages A and B by TMA (128-byte swizzle), mode 1 writes them from registers
 // with the software swizzle (sw128_offset) that the kernels use for built operands.
+// Mode 4 keeps A in tensor memory (written with tcgen05.st, lane m = row m, two bf16 per
+// 32-bit column) and stages B by TMA.
 #include "kda_internal.cuh"
 #include "kda_sm100.cuh"
 
@@ -54,12 +56,28 @@ selftest_mma_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_cons
     tc_fence_after();
     const uint32_t tmem = tmem_base;
     bool ok = true;
+    if (mode == 4) {
+        // A row m -> TMEM lane m (this thread), columns 256 + k/2 (bf16 pairs)
+        const int m = tid;
+        for (int c0 = 0; c0 < K / 2; c0 += 8) {
+            uint32_t v[8];
+            for (int j = 0; j < 8; ++j) {
+                const __nv_bfloat16 lo = A[m * K + 2 * (c0 + j)], hi = A[m * K + 2 * (c0 + j) + 1];
+                v[j] = (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
+            }
+            tmem_st8(tmem_addr(tmem, warp, 256 + c0), v);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    }
 
     if (tid == 0) {
-        if (mode == 0) {
-            mbar_arrive_expect_tx(&bar_full, (uint32_t)(panels * (128 + N) * 128));
+        if (mode == 0 || mode == 4) {
+            mbar_arrive_expect_tx(&bar_full, (uint32_t)(panels * ((mode == 0 ? 128 : 0) + N) * 128));
             for (int p = 0; p < panels; ++p) {
-                tma_load_2d(sa + p * 128 * 128, &tma_a, p * 64, 0, &bar_full);
+                if (mode == 0) tma_load_2d(sa + p * 128 * 128, &tma_a, p * 64, 0, &bar_full);
                 tma_load_2d(sb + p * N * 128, &tma_b, p * 64, 0, &bar_full);
             }
             ok = mbar_wait(&bar_full, 0, status);
@@ -88,7 +106,10 @@ selftest_mma_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_cons
                 const uint64_t bd =
                     b_mn ? desc_sw128_mn(smem_u32(sb + ks * 2048), (uint32_t)K * 128, 1024)
                          : desc_sw128(smem_u32(sb + p * N * 128 + kk * 32));
-                mma_bf16(tmem, ad, bd, idesc, ks > 0 ? 1u : 0u);
+                if (mode == 4)  // A from TMEM: 8 columns (16 bf16) per K step
+                    mma_bf16_ta(tmem, tmem + 256 + ks * 8, bd, idesc, ks > 0 ? 1u : 0u);
+                else
+                    mma_bf16(tmem, ad, bd, idesc, ks > 0 ? 1u : 0u);
             }
         }
         mma_commit(&bar_done);  // arrives even if nothing was issued
@@ -119,7 +140,7 @@ extern "C" kda_status kda_selftest_umma(const void* A, const void* B, float* D, 
                                         int mode, int* status, void* stream) {
     if (!A || !B || !D || !status) return KDA_ERR_INVALID_ARG;
     if (!(N == 16 || N == 32 || N == 64 || N == 128 || N == 256)) return KDA_ERR_UNSUPPORTED;
-    if (K < 16 || K > 128 || K % 16 != 0 || mode < 0 || mode > 3) return KDA_ERR_UNSUPPORTED;
+    if (K < 16 || K > 128 || K % 16 != 0 || mode < 0 || mode > 4) return KDA_ERR_UNSUPPORTED;
     if (mode == 2 && N < 64) return KDA_ERR_UNSUPPORTED;
     CUtensorMap ta, tb;
     const bool a_mn = mode == 3, b_mn = mode == 2;
@@ -132,7 +153,7 @@ extern "C" kda_status kda_selftest_umma(const void* A, const void* B, float* D, 
     if (!ok_a || !ok_b) return KDA_ERR_CUDA;
     // operand area: both readings of the MN-major offsets stay inside these sizes
     const size_t smem = 2 * 128 * 128 + 256 * 128 * 2 + 1024;
-    const uint32_t cols = N < 32 ? 32u : (uint32_t)N;
+    const uint32_t cols = mode == 4 ? 512u : (N < 32 ? 32u : (uint32_t)N);
     cudaFuncSetAttribute(selftest_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     selftest_mma_kernel<<<1, 128, smem, static_cast<cudaStream_t>(stream)>>>(
         ta, tb, static_cast<const __nv_bfloat16*>(A), static_cast<const __nv_bfloat16*>(B), D, N, K,

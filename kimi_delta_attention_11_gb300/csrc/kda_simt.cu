@@ -44,7 +44,7 @@ template <typename Tin, int K, int V>
 __global__ void __launch_bounds__(kThreads)
 kda_intra_simt(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
                const float* __restrict__ g, const float* __restrict__ beta, float scale, int H,
-               const int4* __restrict__ chunk_tab, const int* __restrict__ count,
+               GateArgs ga, const int4* __restrict__ chunk_tab, const int* __restrict__ count,
                float* __restrict__ inter, size_t inter_stride_floats) {
     using S = IntraSmem<K, V>;
     constexpr int C = kChunk, KP = S::KP, VP = S::VP, CP = S::CP;
@@ -70,7 +70,7 @@ kda_intra_simt(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* 
         const size_t off = ((size_t)(t0 + r) * H + h) * K + d;
         qs[r * KP + d] = in ? to_f32(q[off]) : 0.f;
         ks[r * KP + d] = in ? to_f32(k[off]) : 0.f;
-        Gs[r * KP + d] = in ? g[off] : 0.f;
+        Gs[r * KP + d] = in ? gate_log_decay(ga, g[off], h, d, K) : 0.f;
     }
     for (int idx = tid; idx < C * V; idx += kThreads) {
         const int r = idx / V, j = idx % V;
@@ -78,6 +78,28 @@ kda_intra_simt(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* 
     }
     if (tid < C) bs[tid] = tid < len ? beta[(size_t)(t0 + tid) * H + h] : 0.f;
     __syncthreads();
+    if (ga.qk_l2norm) {
+        // rows of q and k divided by max(||.||_2, 1e-6), one warp per row
+        const int warp = tid >> 5, lane = tid & 31;
+        for (int r = warp; r < C; r += kThreads / 32) {
+            float pq = 0.f, pk = 0.f;
+            for (int d = lane; d < K; d += 32) {
+                pq = fmaf(qs[r * KP + d], qs[r * KP + d], pq);
+                pk = fmaf(ks[r * KP + d], ks[r * KP + d], pk);
+            }
+#pragma unroll
+            for (int o2 = 16; o2 > 0; o2 >>= 1) {
+                pq += __shfl_xor_sync(0xffffffffu, pq, o2);
+                pk += __shfl_xor_sync(0xffffffffu, pk, o2);
+            }
+            const float iq = 1.f / fmaxf(sqrtf(pq), 1e-6f), ik = 1.f / fmaxf(sqrtf(pk), 1e-6f);
+            for (int d = lane; d < K; d += 32) {
+                qs[r * KP + d] *= iq;
+                ks[r * KP + d] *= ik;
+            }
+        }
+        __syncthreads();
+    }
 
     // 9.1.3: G^r = log2(e) * sum_{m <= r} g^m within the chunk.
     for (int d = tid; d < K; d += kThreads) {
@@ -287,8 +309,8 @@ kda_h_o_simt(const float* __restrict__ inter, size_t inter_stride_floats,
 
 template <typename T, int K, int V>
 cudaError_t launch_typed(const void* q, const void* k, const void* v, const float* g,
-                         const float* beta, float scale, const float* s0, void* o, float* sN,
-                         int H, const Layout& L, char* ws, cudaStream_t s,
+                         const float* beta, float scale, const GateArgs& ga, const float* s0,
+                         void* o, float* sN, int H, const Layout& L, char* ws, cudaStream_t s,
                          void* const* ev) {
     const size_t stride = L.inter_stride / sizeof(float);
     float* inter = reinterpret_cast<float*>(ws + L.inter_off);
@@ -302,8 +324,8 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v, const floa
         cudaFuncSetAttribute(kin, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         dim3 grid((unsigned)L.max_chunks, (unsigned)H);
         kin<<<grid, kThreads, smem, s>>>(static_cast<const T*>(q), static_cast<const T*>(k),
-                                         static_cast<const T*>(v), g, beta, scale, H, ctab, count,
-                                         inter, stride);
+                                         static_cast<const T*>(v), g, beta, scale, H, ga, ctab,
+                                         count, inter, stride);
         if (cudaError_t e = cudaGetLastError()) return e;
     }
     if (!record_event(ev, 0, s)) return cudaErrorInvalidResourceHandle;
@@ -323,12 +345,12 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v, const floa
 }  // namespace
 
 cudaError_t launch_simt(const void* q, const void* k, const void* v, const float* g,
-                        const float* beta, float scale, const float* s0, void* o, float* sN,
-                        int H, int K, int V, kda_dtype dt, const Layout& L, char* ws,
-                        cudaStream_t s, void* const* ev) {
+                        const float* beta, float scale, const GateArgs& ga, const float* s0,
+                        void* o, float* sN, int H, int K, int V, kda_dtype dt, const Layout& L,
+                        char* ws, cudaStream_t s, void* const* ev) {
 #define KDA_SIMT_CASE(T_, K_, V_)                                                               \
     if (K == K_ && V == V_)                                                                     \
-        return launch_typed<T_, K_, V_>(q, k, v, g, beta, scale, s0, o, sN, H, L, ws, s, ev);
+        return launch_typed<T_, K_, V_>(q, k, v, g, beta, scale, ga, s0, o, sN, H, L, ws, s, ev);
     if (dt == KDA_DTYPE_F32) {
         KDA_SIMT_CASE(float, 64, 64)
         KDA_SIMT_CASE(float, 64, 128)

@@ -98,6 +98,19 @@ __device__ __forceinline__ void st8f(float* p, const float (&f)[8]) {
     q[1] = make_float4(f[4], f[5], f[6], f[7]);
 }
 
+// Divides a row of 128 channels, held as 8 channels by each of 16 consecutive lanes, by
+// max(||row||_2, 1e-6) ("KDAChunkwise", FP32 core: F.normalize with eps 1e-6).
+__device__ __forceinline__ void l2_scale_row(float (&x)[8]) {
+    float ss = 0.f;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) ss = fmaf(x[m], x[m], ss);
+#pragma unroll
+    for (int o2 = 8; o2 > 0; o2 >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o2);
+    const float inv = 1.f / fmaxf(sqrtf(ss), 1e-6f);
+#pragma unroll
+    for (int m = 0; m < 8; ++m) x[m] *= inv;
+}
+
 // index of the block pair (b, b'), b' < b, in the table of 2^{G_16b - G_16b'}
 __device__ __forceinline__ int pair_index(int b, int bp) { return b * (b - 1) / 2 + bp; }
 
@@ -141,12 +154,15 @@ static_assert(IntraMap::LF + 64 * kLs * 4 <= IntraMap::RA + 32768, "L tile overf
 static_assert(IntraMap::JB + 6 * 16 * kBs * 4 <= IntraMap::AIA, "J blocks overflow");
 static_assert(4 * 16 * kBs * 4 <= IntraMap::END - IntraMap::MISC, "X blocks overflow");
 
+// kOpts: the in-kernel gate activation / q-k normalisation are compiled in (a separate
+// instantiation, so the plain kernel carries none of their code or registers).
+template <bool kOpts>
 __global__ void __launch_bounds__(kIntraThreads, 2)
 kda_intra_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
-             const float* __restrict__ beta, float scale, int H, const int4* __restrict__ chunk_tab,
-             const int2* __restrict__ seq_tab, const int* __restrict__ count, long long max_chunks,
-             RangeArgs ra, uint8_t* __restrict__ records, int* __restrict__ status) {
+             const float* __restrict__ beta, float scale, GateArgs ga, int H, ChunkIndex cx,
+             long long max_chunks, RangeArgs ra, uint8_t* __restrict__ records,
+             int* __restrict__ status) {
     using M = IntraMap;
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t bar_tma, bar_rel, bar_wu;
@@ -160,18 +176,18 @@ kda_intra_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         // whole problem: chunks from the last to the first, so that the records of early
         // chunks, which the recurrence reads first, are the most recently written
         c = max_chunks - 1 - blk / H;
-        if (c >= *count) return;
+        if (c >= cx.num_chunks(max_chunks)) return;
         slot = c;
     } else {
         // chunks j0 <= j < j0 + span of every sequence (j = index within the sequence)
         const long long rest = blk / H;
         const int jj = (int)(rest % ra.span), n = (int)(rest / ra.span);
-        const int2 sq = seq_tab[n];
+        const int2 sq = cx.seq(n);
         if (ra.j0 + jj >= sq.y) return;
         c = sq.x + ra.j0 + jj;
         slot = (long long)n * ra.span + jj;
     }
-    const int4 ent = chunk_tab[c];
+    const int4 ent = cx.chunk(c);
     const int t0 = ent.y, len = ent.z;
     uint8_t* rec = records + ((size_t)slot * H + h) * TcRecord::bytes;
 
@@ -229,6 +245,10 @@ kda_intra_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         for (int r = 0; r < 4; ++r) {
             const int i = 4 * rg + r;
             ld8f(gt + i * 128 + dc * 8, swap, G[r]);
+            if (kOpts && ga.mode != 0) {  // raw gate -> ln(alpha) (Tokamax design doc 9.1.3)
+#pragma unroll
+                for (int m = 0; m < 8; ++m) G[r][m] = gate_log_decay(ga, G[r][m], h, dc * 8 + m, 128);
+            }
             if (i >= len) {
 #pragma unroll
                 for (int m = 0; m < 8; ++m) G[r][m] = 0.f;
@@ -322,6 +342,7 @@ kda_intra_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 const uint32_t a = M::RB + (grp * 2 + P) * 8192 + sw128_chunk(ii, cc);
                 float qv[8], qs[8], qg[8];
                 unpack8(qr[r & 1], qv);
+                if (kOpts && ga.qk_l2norm) l2_scale_row(qv);
 #pragma unroll
                 for (int m = 0; m < 8; ++m) {
                     qs[m] = scale * qv[m] * inb * e[m];
@@ -336,6 +357,7 @@ kda_intra_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 const uint32_t a = M::KT + P * 8192 + sw128_chunk(i, cc);
                 float kv[8], kp[8], kpl[8], kb[8];
                 unpack8(kr[r & 1], kv);
+                if (kOpts && ga.qk_l2norm) l2_scale_row(kv);
 #pragma unroll
                 for (int m = 0; m < 8; ++m) {
                     kv[m] *= inb;
@@ -682,8 +704,7 @@ static_assert(TcRecord::u1 == 0 && TcRecord::u0 == kStage && TcRecord::gamma == 
               "record layout assumed by the recurrence kernel");
 
 __global__ void __launch_bounds__(kHoThreads, 1)
-kda_h_o_tc(const uint8_t* __restrict__ records, const int4* __restrict__ chunk_tab,
-           const int2* __restrict__ seq_tab, long long max_chunks, RangeArgs ra,
+kda_h_o_tc(const uint8_t* __restrict__ records, ChunkIndex cx, long long max_chunks, RangeArgs ra,
            const float* __restrict__ s0, __nv_bfloat16* __restrict__ o, float* __restrict__ sN,
            int H, int* __restrict__ status) {
     using M = HoMap;
@@ -699,7 +720,7 @@ kda_h_o_tc(const uint8_t* __restrict__ records, const int4* __restrict__ chunk_t
     uint8_t* sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
     const uint32_t sb = smem_u32(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int2 sq = seq_tab[n];
+    const int2 sq = cx.seq(n);
     int seq_chunks = sq.y;
     if ((long long)sq.x + seq_chunks > max_chunks) {  // inconsistent cu_seqlens: stop rather than overrun
         if (tid == 0) atomicCAS(status, 0, (int)KDA_ERR_INVALID_ARG);
@@ -843,7 +864,7 @@ kda_h_o_tc(const uint8_t* __restrict__ records, const int4* __restrict__ chunk_t
             tc_fence_after();
             float ov[32];
             tmem_ld32(tmem_addr(tmem + 64 * (ci & 1), qd, 32 * half), ov);
-            const int4 ent = chunk_tab[first + ci];
+            const int4 ent = cx.chunk(first + ci);
             const int i = d - 64;
             if (i < ent.z) {
                 uint4* dst = reinterpret_cast<uint4*>(o + ((size_t)(ent.y + i) * H + h) * 128 +
@@ -870,8 +891,15 @@ kda_h_o_tc(const uint8_t* __restrict__ records, const int4* __restrict__ chunk_t
             if (!__all_sync(0xffffffffu,
                             mbar_wait_abortable(&full[sg], (ci / kStages) & 1, status, abort_flag)))
                 break;
-            // the previous chunk's output is read while MMA1 runs
+            // the previous chunk's output is read while MMA1 runs; U rows are fetched
+            // before MMA1 completes
             if (qd >= 2 && ci > 0) emit_output(ci - 1);
+            uint4 ur[4];
+            if (qd < 2) {
+                const uint32_t ub = (uint32_t)sg * kStage + UO;
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) ur[q4] = lds128(sm, ub + sw128_chunk(d, 4 * half + q4));
+            }
             if (!__all_sync(0xffffffffu, mbar_wait_abortable(&bar_m1, ci & 1, status, abort_flag)))
                 break;
             tc_fence_after();
@@ -879,10 +907,6 @@ kda_h_o_tc(const uint8_t* __restrict__ records, const int4* __restrict__ chunk_t
                 // ep1: V_new[i] = U[i] - (W S)[i], token i = TMEM lane = d, 32 columns
                 float ws[32];
                 tmem_ld32(tmem_addr(D1, qd, 32 * half), ws);
-                const uint32_t ub = (uint32_t)sg * kStage + UO;
-                uint4 ur[4];
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) ur[q4] = lds128(sm, ub + sw128_chunk(d, 4 * half + q4));
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
                     float uf[8], vn[8];
@@ -963,13 +987,19 @@ cudaError_t pipe_res(int dev, PipeRes** out) {
 }  // namespace
 
 cudaError_t launch_tc(const void* q, const void* k, const void* v, const float* g,
-                      const float* beta, float scale, const float* s0, void* o, float* sN, int B,
-                      int T, int H, const Layout& L, char* ws, cudaStream_t s,
+                      const float* beta, float scale, const GateArgs& ga, const float* s0, void* o,
+                      float* sN, int B, int T, int H, const Layout& L, char* ws, cudaStream_t s,
                       void* const* ev) {
     uint8_t* records = reinterpret_cast<uint8_t*>(ws + L.inter_off);
-    const int4* ctab = reinterpret_cast<const int4*>(ws + L.chunk_tab_off);
-    const int2* stab = reinterpret_cast<const int2*>(ws + L.seq_tab_off);
-    const int* count = reinterpret_cast<const int*>(ws + L.count_off);
+    ChunkIndex cx;
+    cx.chunk_tab = reinterpret_cast<const int4*>(ws + L.chunk_tab_off);
+    cx.seq_tab = reinterpret_cast<const int2*>(ws + L.seq_tab_off);
+    cx.count = reinterpret_cast<const int*>(ws + L.count_off);
+    if (L.fixed) {
+        cx.fixed = 1;
+        cx.T = T;
+        cx.nct = (T + kChunk - 1) / kChunk;
+    }
     int* status = reinterpret_cast<int*>(ws + L.status_off);
     CUtensorMap tq, tk, tv, tg;
     if (L.max_chunks > 0) {
@@ -979,11 +1009,14 @@ cudaError_t launch_tc(const void* q, const void* k, const void* v, const float* 
             !make_tmap_2d(&tv, v, true, inner, rows, inner * 2, 64, 64, true) ||
             !make_tmap_2d(&tg, g, false, inner, rows, inner * 4, 128, 64, false))
             return cudaErrorInvalidValue;
-        cudaFuncSetAttribute(kda_intra_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(kda_intra_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kIntraSmem);
+        cudaFuncSetAttribute(kda_intra_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kIntraSmem);
     }
     cudaFuncSetAttribute(kda_h_o_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kHoSmem);
     __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(o);
+    auto* intra = (ga.mode != 0 || ga.qk_l2norm) ? kda_intra_tc<true> : kda_intra_tc<false>;
     const unsigned ho_blocks = (unsigned)L.N * H * 2;
 
     // Whole-problem schedule: one launch of each kernel (and the only one with per-kernel
@@ -991,15 +1024,14 @@ cudaError_t launch_tc(const void* q, const void* k, const void* v, const float* 
     if (L.span == 0 || ev) {
         if (L.max_chunks > 0) {
             const unsigned blocks = (unsigned)(L.max_chunks * H);
-            kda_intra_tc<<<blocks, kIntraThreads, kIntraSmem, s>>>(
-                tq, tk, tv, tg, beta, scale, H, ctab, stab, count, L.max_chunks, RangeArgs{},
-                records, status);
+            intra<<<blocks, kIntraThreads, kIntraSmem, s>>>(
+                tq, tk, tv, tg, beta, scale, ga, H, cx, L.max_chunks, RangeArgs{}, records, status);
             if (cudaError_t e = cudaGetLastError()) return e;
         }
         if (!record_event(ev, 0, s)) return cudaErrorInvalidResourceHandle;
         if (L.N > 0) {
-            kda_h_o_tc<<<ho_blocks, kHoThreads, kHoSmem, s>>>(records, ctab, stab, L.max_chunks,
-                                                              RangeArgs{}, s0, ob, sN, H, status);
+            kda_h_o_tc<<<ho_blocks, kHoThreads, kHoSmem, s>>>(records, cx, L.max_chunks, RangeArgs{},
+                                                              s0, ob, sN, H, status);
             if (cudaError_t e = cudaGetLastError()) return e;
         }
         if (!record_event(ev, 1, s)) return cudaErrorInvalidResourceHandle;
@@ -1026,13 +1058,13 @@ cudaError_t launch_tc(const void* q, const void* k, const void* v, const float* 
         const RangeArgs ra{r * L.span, L.span, carry};
         if (r >= L.ring)
             if (cudaError_t e = cudaStreamWaitEvent(s, P->ho_done[sl], 0)) return e;
-        kda_intra_tc<<<(unsigned)(L.N * L.span * H), kIntraThreads, kIntraSmem, s>>>(
-            tq, tk, tv, tg, beta, scale, H, ctab, stab, count, L.max_chunks, ra, rec, status);
+        intra<<<(unsigned)(L.N * L.span * H), kIntraThreads, kIntraSmem, s>>>(
+            tq, tk, tv, tg, beta, scale, ga, H, cx, L.max_chunks, ra, rec, status);
         if (cudaError_t e = cudaGetLastError()) return e;
         if (cudaError_t e = cudaEventRecord(P->intra_done[sl], s)) return e;
         if (cudaError_t e = cudaStreamWaitEvent(P->side, P->intra_done[sl], 0)) return e;
-        kda_h_o_tc<<<ho_blocks, kHoThreads, kHoSmem, P->side>>>(rec, ctab, stab, L.max_chunks, ra,
-                                                                 s0, ob, sN, H, status);
+        kda_h_o_tc<<<ho_blocks, kHoThreads, kHoSmem, P->side>>>(rec, cx, L.max_chunks, ra, s0,
+                                                                 ob, sN, H, status);
         if (cudaError_t e = cudaGetLastError()) return e;
         if (cudaError_t e = cudaEventRecord(P->ho_done[sl], P->side)) return e;
     }

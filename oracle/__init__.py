@@ -3,8 +3,9 @@
 TEST INFRASTRUCTURE.  Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline
 leg of ``bench.py`` import this package.  The CUDA library never calls it and shares no
 code with it: ``kda_oracle.c`` is a plain C restatement of the token recurrence
-(Tokamax "chunk_kda_fwd_design_doc", Appendix 9.1.2, Eq. (1)) and of the chunkwise form
-(same document, 9.1.3-9.1.6, Eq. (6)-(9)).
+(Tokamax "chunk_kda_fwd_design_doc", Appendix 9.1.2, Eq. (1)), of the chunkwise form
+(same document, 9.1.3-9.1.6, Eq. (6)-(9)), of the raw-gate activation (9.1.3) and of the
+q/k row normalisation (Kimi-K3 docs, "KDAChunkwise", FP32 core).
 
 Every function here is pinned by ``tests/pins.py``; ``tests/test_oracle_mutants.py``
 plants single mistakes in a copy of the C source and checks that a pin catches each.
@@ -69,7 +70,36 @@ class Oracle:
         self.lib.kda_oracle_recurrent.restype = ctypes.c_int
         self.lib.kda_oracle_chunkwise.argtypes = common + [ctypes.c_int, dp, dp, ctypes.c_int]
         self.lib.kda_oracle_chunkwise.restype = ctypes.c_int
+        self.lib.kda_oracle_gate.argtypes = [dp, dp, dp, ctypes.c_double, ctypes.c_long,
+                                             ctypes.c_int, ctypes.c_int, dp]
+        self.lib.kda_oracle_gate.restype = ctypes.c_int
+        self.lib.kda_oracle_l2norm.argtypes = [dp, ctypes.c_long, ctypes.c_int, ctypes.c_double, dp]
+        self.lib.kda_oracle_l2norm.restype = ctypes.c_int
         self.threads_used = 0
+
+    def gate(self, x, a_log, dt_bias=None, lower_bound=0.0):
+        """ln(alpha) from a raw gate x [..., H, K] (Tokamax design doc 9.1.3)."""
+        xa = _f64(x)
+        H, K = xa.shape[-2], xa.shape[-1]
+        rows = xa.size // (H * K)
+        al = _f64(a_log).reshape(H)
+        db = None if dt_bias is None else _f64(dt_bias).reshape(H * K)
+        out = np.empty_like(xa)
+        rc = self.lib.kda_oracle_gate(_ptr(xa), _ptr(al), _ptr(db), float(lower_bound), rows, H, K,
+                                      _ptr(out))
+        if rc < 0:
+            raise ValueError("kda_oracle_gate: invalid arguments")
+        return out
+
+    def l2norm(self, x, eps=1e-6):
+        """x / max(||x||_2, eps) along the last dimension ("KDAChunkwise", F.normalize)."""
+        xa = _f64(x)
+        D = xa.shape[-1]
+        out = np.empty_like(xa)
+        rc = self.lib.kda_oracle_l2norm(_ptr(xa), xa.size // D, D, float(eps), _ptr(out))
+        if rc < 0:
+            raise ValueError("kda_oracle_l2norm: invalid arguments")
+        return out
 
     def _prepare(self, q, k, v, g, beta, initial_state, cu_seqlens):
         q, k, v, g, beta = (_f64(t) for t in (q, k, v, g, beta))

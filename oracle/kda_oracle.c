@@ -388,3 +388,48 @@ int kda_oracle_chunkwise(const double* q, const double* k, const double* v,
         return -1;
     return run(&J, chunkwise_unit, num_threads);
 }
+
+/* ------------------------------------------------------------------------------------
+ * Gate activation and row normalisation (the inputs of use_gate_in_kernel / q-k
+ * normalisation; applied before the recurrence, which then takes ell = ln(alpha)).
+ * ------------------------------------------------------------------------------------ */
+
+/* softplus(y) = ln(1 + e^y), evaluated as max(y, 0) + ln(1 + e^{-|y|}) (the same value,
+ * without overflow of e^y for large y). */
+static double softplus(double y) {
+    const double a = y > 0.0 ? y : -y;
+    return (y > 0.0 ? y : 0.0) + log1p(exp(-a));
+}
+
+/* sigmoid(y) = 1 / (1 + e^{-y}). */
+static double sigmoid(double y) { return 1.0 / (1.0 + exp(-y)); }
+
+int kda_oracle_gate(const double* x, const double* a_log, const double* dt_bias,
+                    double lower_bound, long rows, int H, int K, double* ell) {
+    if (!x || !a_log || !ell || rows < 0 || H < 1 || K < 1) return -1;
+    for (long r = 0; r < rows; ++r) {
+        for (int h = 0; h < H; ++h) {
+            const double lam = exp(a_log[h]);
+            for (int d = 0; d < K; ++d) {
+                const size_t i = ((size_t)r * H + h) * K + d;
+                double xb = x[i];
+                if (dt_bias) xb += dt_bias[(size_t)h * K + d];
+                ell[i] = lower_bound == 0.0 ? -lam * softplus(xb) : lower_bound * sigmoid(lam * xb);
+            }
+        }
+    }
+    return 1;
+}
+
+int kda_oracle_l2norm(const double* x, long rows, int D, double eps, double* y) {
+    if (!x || !y || rows < 0 || D < 1) return -1;
+    for (long r = 0; r < rows; ++r) {
+        const double* xr = x + (size_t)r * D;
+        double ss = 0.0;
+        for (int d = 0; d < D; ++d) ss += xr[d] * xr[d];
+        double n = sqrt(ss);
+        if (n < eps) n = eps;
+        for (int d = 0; d < D; ++d) y[(size_t)r * D + d] = xr[d] / n;
+    }
+    return 1;
+}

@@ -58,6 +58,18 @@ int kda_oracle_chunkwise(const double* q, const double* k, const double* v,
                          int chunk_size, double* o, double* final_state,
                          int num_threads);
 
+/* Gate activation of a raw gate, [TKD] 9.1.3 (use_gate_in_kernel):
+ *   x' = x + dt_bias[h][d] (dt_bias nullable, [H][K]), lambda_h = exp(a_log[h]);
+ *   lower_bound == 0:  ell = -lambda_h * softplus(x'),  softplus(y) = ln(1 + e^y);
+ *   otherwise:         ell = lower_bound * sigmoid(lambda_h x'),  sigmoid(y) = 1/(1+e^-y).
+ * x and ell are [rows][H][K] (rows = B * T).  Returns 1, or -1 for invalid arguments. */
+int kda_oracle_gate(const double* x, const double* a_log, const double* dt_bias,
+                    double lower_bound, long rows, int H, int K, double* ell);
+
+/* Row normalisation along the last dimension, [KCW] "FP32 core and log-space decay"
+ * (F.normalize): y = x / max(||x||_2, eps).  x, y: [rows][D].  Returns 1 or -1. */
+int kda_oracle_l2norm(const double* x, long rows, int D, double eps, double* y);
+
 #ifdef __cplusplus
 }
 #endif

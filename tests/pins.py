@@ -10,7 +10,8 @@ Sources (web pages, by title and section):
   form), 9.1.3-9.1.6 (chunkwise Eq. (6)-(9)), 9.1.7 (variable-length sequences);
   "KDA Doesn't Care About the Future", "Chunkwise KDA in Broad Strokes" and
   "Decisions Decisions" (causality); Kimi-K3 "KDAChunkwise", "Verification and
-  boundaries" (chunkwise-vs-recurrent test idea, chunk sizes 1, 2, 4, 8).
+  boundaries" (chunkwise-vs-recurrent test idea, chunk sizes 1, 2, 4, 8) and "FP32 core
+  and log-space decay" (q/k normalisation); Tokamax 9.1.3 and 5.3 (raw-gate forms).
 """
 from __future__ import annotations
 
@@ -279,6 +280,71 @@ def pin_varlen_isolation(oracle, forms=(RECURRENT, 64)):
             assert np.array_equal(fin[n:n + 1], f1), f"sequence {n} state differs when packed"
 
 
+def pin_gate_softplus(oracle):
+    """Raw-gate softplus form (Tokamax design doc 9.1.3): ell = -exp(a_log) softplus(x + b).
+    Facts of the mathematics: softplus(y) - softplus(-y) = y exactly in value, softplus(0)
+    = ln 2, softplus(y) -> 0 for y -> -inf (the design doc's -1e4 raw-gate padding gives
+    an identity decay), ell <= 0, ell is linear in exp(a_log), and dt_bias shifts x."""
+    rng = np.random.default_rng(11)
+    H, K = 3, 5
+    x = rng.standard_normal((4, H, K)) * 3.0
+    a_log = np.array([0.0, math.log(2.0), -0.7])
+    b = rng.standard_normal(H * K)
+    lam = np.exp(a_log)[None, :, None]
+    e_pos = oracle.gate(x, a_log, None, 0.0)
+    e_neg = oracle.gate(-x, a_log, None, 0.0)
+    # -ell / lam = softplus(x): softplus(x) - softplus(-x) = x
+    assert np.allclose(-e_pos / lam + e_neg / lam, x, rtol=0, atol=1e-13)
+    assert np.all(e_pos <= 0.0)
+    z = oracle.gate(np.zeros((1, H, K)), a_log, None, 0.0)
+    assert np.allclose(z, -np.exp(a_log)[None, :, None] * math.log(2.0), rtol=0, atol=1e-15)
+    pad = oracle.gate(np.full((1, H, K), -1e4), a_log, None, 0.0)
+    assert np.all(np.abs(pad) < 1e-300)
+    # exp(a_log) = 2 doubles the decay of exp(a_log) = 1
+    assert np.allclose(e_pos[:, 1], 2.0 * oracle.gate(x, np.zeros(H), None, 0.0)[:, 1], atol=1e-14)
+    # dt_bias adds to x before the activation
+    shifted = x + b.reshape(H, K)[None]
+    assert np.allclose(oracle.gate(x, a_log, b, 0.0), oracle.gate(shifted, a_log, None, 0.0),
+                       rtol=0, atol=1e-14)
+
+
+def pin_gate_sigmoid(oracle):
+    """Lower-bound form (Tokamax design doc 9.1.3, 5.3): ell = a sigmoid(exp(a_log)(x + b))
+    with -5 <= a < 0.  Facts: sigmoid(y) + sigmoid(-y) = 1, sigmoid(0) = 1/2, so ell lies in
+    (a, 0), ell(x) + ell(-x) = a, ell(0) = a / 2, ell decreases with x, and exp(a_log)
+    scales x."""
+    rng = np.random.default_rng(12)
+    H, K, a = 2, 6, -3.5
+    x = rng.standard_normal((5, H, K)) * 2.0
+    a_log = np.array([0.3, -1.2])
+    e = oracle.gate(x, a_log, None, a)
+    assert np.all((e < 0.0) & (e > a))
+    assert np.allclose(e + oracle.gate(-x, a_log, None, a), a, rtol=0, atol=1e-14)
+    assert np.allclose(oracle.gate(np.zeros((1, H, K)), a_log, None, a), a / 2, rtol=0, atol=1e-15)
+    xs = np.sort(x, axis=0)
+    es = oracle.gate(xs, a_log, None, a)
+    assert np.all(np.diff(es, axis=0) <= 0.0)
+    lam = np.exp(a_log)[None, :, None]
+    assert np.allclose(e, oracle.gate(x * lam, np.zeros(H), None, a), rtol=0, atol=1e-14)
+    b = rng.standard_normal(H * K)
+    assert np.allclose(oracle.gate(x, a_log, b, a),
+                       oracle.gate(x + b.reshape(H, K)[None], a_log, None, a), rtol=0, atol=1e-14)
+
+
+def pin_l2norm(oracle):
+    """x / max(||x||_2, eps) ("KDAChunkwise", F.normalize with eps 1e-6): rows of norm
+    >= eps come out with norm 1 and the direction of x, a 3-4-5 row is exact, rows below
+    eps are divided by eps, the zero row stays zero."""
+    rng = np.random.default_rng(13)
+    x = rng.standard_normal((7, 9)) * rng.uniform(0.1, 10.0, (7, 1))
+    y = oracle.l2norm(x)
+    assert np.allclose(np.linalg.norm(y, axis=1), 1.0, rtol=0, atol=1e-14)
+    assert np.allclose(y * np.linalg.norm(x, axis=1, keepdims=True), x, rtol=1e-14, atol=0)
+    assert np.array_equal(oracle.l2norm(np.array([[3.0, 4.0]])), np.array([[0.6, 0.8]]))
+    tiny = np.array([[3e-8, 4e-8], [0.0, 0.0]])
+    assert np.allclose(oracle.l2norm(tiny), [[3e-2, 4e-2], [0.0, 0.0]], rtol=1e-14, atol=0)
+
+
 ALL_PINS = [
     pin_eq1_exact_rational,
     pin_linear_attention,
@@ -288,4 +354,7 @@ ALL_PINS = [
     pin_causality,
     pin_split_resume,
     pin_varlen_isolation,
+    pin_gate_softplus,
+    pin_gate_sigmoid,
+    pin_l2norm,
 ]

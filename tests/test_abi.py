@@ -42,16 +42,17 @@ def test_status_strings(lib):
 
 
 def test_launch_count(lib):
-    """Whole-problem schedule: 3 launches; pipelined (bf16 K = V = 128, fixed length,
-    <= 128 chains, >= 512 chunks per sequence): chunk index + 2 per range of 32 chunks."""
+    """bf16 K = V = 128 fixed length: no index kernel, intra + recurrence (once per range
+    of 32 chunks when pipelined: <= 128 chains, >= 512 chunks per sequence); packed input
+    and the other paths: index + intra + recurrence."""
     lc = lambda *a: lib.kda_fwd_launch_count(*a)
     bf16, f32 = 0, 1
-    assert lc(2, 4096, 16, 128, 128, 0, 64, bf16) == 3             # 64 chunks
-    assert lc(1, 131072, 32, 128, 128, 0, 64, bf16) == 1 + 2 * 64  # 2048 chunks
-    assert lc(1, 512 * 64, 2, 128, 128, 0, 64, bf16) == 1 + 2 * 16
-    assert lc(1, 511 * 64, 2, 128, 128, 0, 64, bf16) == 3          # 511 chunks
-    assert lc(1, 600 * 64 + 5, 2, 128, 128, 0, 64, bf16) == 1 + 2 * 19
-    assert lc(32, 2048, 32, 128, 128, 0, 64, bf16) == 3            # 1024 chains
+    assert lc(2, 4096, 16, 128, 128, 0, 64, bf16) == 2             # 64 chunks
+    assert lc(1, 131072, 32, 128, 128, 0, 64, bf16) == 2 * 64      # 2048 chunks
+    assert lc(1, 512 * 64, 2, 128, 128, 0, 64, bf16) == 2 * 16
+    assert lc(1, 511 * 64, 2, 128, 128, 0, 64, bf16) == 2          # 511 chunks
+    assert lc(1, 600 * 64 + 5, 2, 128, 128, 0, 64, bf16) == 2 * 19
+    assert lc(32, 2048, 32, 128, 128, 0, 64, bf16) == 2            # 1024 chains
     assert lc(1, 37000, 32, 128, 128, 8, 64, bf16) == 3            # packed
     assert lc(1, 131072, 32, 128, 128, 0, 64, f32) == 3            # fp32 path
     assert lc(1, 131072, 32, 64, 64, 0, 64, bf16) == 3             # other shapes
@@ -129,3 +130,39 @@ def test_chunk_index_rejects(lib):
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(kda.KdaLibraryMissing):
         _native.load_library(str(tmp_path / "missing.so"))
+
+
+def call_decode(lib, opts=None, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, scale=0.1, state=FAKE, o=FAKE, N=2, H=1,
+             K=64, V=64, dt=1, stream=None)
+    a.update(kw)
+    return lib.kda_decode(a["q"], a["k"], a["v"], a["g"], a["beta"], a["scale"], a["state"],
+                          a["o"], a["N"], a["H"], a["K"], a["V"], a["dt"],
+                          None if opts is None else ctypes.byref(opts), a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), INVALID), (dict(state=None), INVALID), (dict(o=None), INVALID),
+    (dict(N=-1), INVALID), (dict(H=0), INVALID), (dict(dt=5), INVALID), (dict(K=512), INVALID),
+    (dict(K=96), UNSUPPORTED), (dict(V=32), UNSUPPORTED),
+    (dict(q=FAKE + 2), ALIGN), (dict(state=FAKE + 2), ALIGN), (dict(beta=FAKE + 1), ALIGN),
+    (dict(N=0, q=None, state=None), OK),      # nothing to do
+])
+def test_decode_rejects_before_launch(lib, kw, status):
+    assert call_decode(lib, **kw) == status
+
+
+@pytest.mark.parametrize("fields,status", [
+    (dict(use_gate_in_kernel=1, a_log=None), INVALID),              # a_log required
+    (dict(use_gate_in_kernel=1, a_log=FAKE, lower_bound=-6.0), INVALID),
+    (dict(use_gate_in_kernel=1, a_log=FAKE, lower_bound=0.5), INVALID),
+    (dict(use_gate_in_kernel=1, a_log=FAKE + 2), ALIGN),
+    (dict(use_gate_in_kernel=1, a_log=FAKE, dt_bias=FAKE + 1), ALIGN),
+])
+def test_gate_options_validated(lib, fields, status):
+    opts = _native._GateOptions(**{"use_gate_in_kernel": 0, "a_log": None, "dt_bias": None,
+                                   "lower_bound": 0.0, "qk_l2norm": 0, **fields})
+    assert call_decode(lib, opts) == status
+    a = [FAKE, FAKE, FAKE, FAKE, FAKE, 0.1, 64, None, None, 0, FAKE, None, 1, 64, 1, 64, 64, 1,
+         FAKE, 1 << 40]
+    assert lib.kda_fwd_ex(*a, ctypes.byref(opts), None) == status

@@ -64,6 +64,15 @@ MUTANTS = {
                             "J->scale * Q_(r, d) * S[(size_t)d * V + jv]")],
     "state_without_decay": [("= gammaC * S[(size_t)d * V + jv] + acc;",
                              "= S[(size_t)d * V + jv] + acc;")],
+    # raw-gate activation and row normalisation
+    "softplus_sign": [("log1p(exp(-a))", "log1p(exp(a))")],
+    "softplus_no_linear_part": [("return (y > 0.0 ? y : 0.0) + log1p", "return log1p")],
+    "sigmoid_sign": [("1.0 / (1.0 + exp(-y))", "1.0 / (1.0 + exp(y))")],
+    "gate_without_lambda": [("-lam * softplus(xb)", "-softplus(xb)")],
+    "sigmoid_without_lambda": [("lower_bound * sigmoid(lam * xb)", "lower_bound * sigmoid(xb)")],
+    "gate_without_bias": [("if (dt_bias) xb += dt_bias[(size_t)h * K + d];", "")],
+    "l2norm_without_eps": [("if (n < eps) n = eps;", "")],
+    "l2norm_without_sqrt": [("double n = sqrt(ss);", "double n = ss;")],
 }
 
 

@@ -58,6 +58,35 @@ WORKLOADS: Dict[str, Workload] = {
 }
 
 
+# Decode-step workload: one token for each of N sequences against an existing state (the
+# serving batch of the measurement plan, 32 sequences x 32 heads).
+DECODE_WORKLOADS: Dict[str, dict] = {
+    "decode_bf16": dict(N=32, H=32, K=128, V=128, dtype=torch.bfloat16, init_std=0.1, seed=1006),
+}
+
+
+def make_decode_inputs(N: int, H: int, K: int, V: int, dtype: torch.dtype, init_std: float,
+                       seed: int, device: str = "cpu") -> Dict[str, object]:
+    """q, k [N,H,K] (unit rows), v [N,H,V], g [N,H,K] = -5 sigmoid(N(0,1)), beta [N,H] =
+    sigmoid(N(0,1)), state [N,H,K,V] ~ N(0, init_std^2), by the shared recipe."""
+    gen = torch.Generator().manual_seed(seed)
+
+    def unit_rows(shape):
+        x = torch.randn(shape, generator=gen, dtype=torch.float32)
+        return x / x.norm(dim=-1, keepdim=True).clamp_min(1e-6)
+
+    out = dict(q=unit_rows((N, H, K)).to(dtype), k=unit_rows((N, H, K)).to(dtype),
+               v=torch.randn((N, H, V), generator=gen).to(dtype),
+               g=(-5.0 * torch.sigmoid(torch.randn((N, H, K), generator=gen))).contiguous(),
+               beta=torch.sigmoid(torch.randn((N, H), generator=gen)).contiguous(),
+               state=(init_std * torch.randn((N, H, K, V), generator=gen)).contiguous(),
+               scale=K ** -0.5, N=N, H=H, K=K, V=V, dtype=dtype)
+    if device != "cpu":
+        for key in ("q", "k", "v", "g", "beta", "state"):
+            out[key] = out[key].to(device)
+    return out
+
+
 def custom(name: str = "custom", **kw) -> Workload:
     """A workload with the shared recipe and explicit sizes (for small test cases)."""
     base = dict(B=1, T=128, H=1, K=64, V=64, dtype=torch.float32, seed=7)
