@@ -119,21 +119,39 @@ struct SimtRecord {
 
 // Per-(chunk, head) record of the bf16 tensor-core path (K = V = 128).  Every tile is
 // stored as the exact shared-memory image the recurrence kernel feeds to tcgen05 (128-byte
-// swizzled 64-element panels), so that kernel fetches it with plain bulk copies.
-//   u1     U, values 64-127: [64 tokens][64] token-major.                         8 KB
+// swizzled 64-element panels), so that kernel fetches the record with one bulk copy.
+// The recurrence computes transposed products (state and V_new as tensor-memory operands
+// with one lane per value column), so every tile here is its B operand:
 //   wq     [W ; Qg]  2 panels (key 0-63, 64-127) x [128 rows][64], K-major: rows 0-63 W
 //                    (one per token), rows 64-127 the gated, scaled query.    32 KB
 //   aqk    Aqk       [64 query rows][64 key cols], K-major, zero above the diagonal. 8 KB
-//                    (rows 64-127 of panel 1 of wq followed by aqk form a 128-row A
-//                    operand whose upper half only feeds accumulator rows the
-//                    recurrence has already consumed.)
-//   kb0, kb1  K_bar  keys 0-63 / 64-127: [64 tokens][64] token-major (read by the tensor
-//                    core as the transposed operand K_bar^T).                   16 KB
-//   u0     U, values 0-63.                                                       8 KB
+//   kb0, kb1  K_bar  keys 0-63 / 64-127: [64 tokens][64] token-major (MN-major B).  16 KB
+//   ut     U^T       [128 value rows][64 tokens], K-major.                         16 KB
 //   gamma  gamma^C   [128] fp32 (decay of the whole chunk per key channel).
-// The recurrence kernel's CTA for value slice s fetches one contiguous run per chunk:
-// [u1, u0) for s = 1 and [wq, gamma) for s = 0 (one large copy beats several small ones).
+// (Records for the value-sliced recurrence kernel, which computes the untransposed
+// products with a state slice of 64 value columns per CTA, use TcRecordS below.)
 struct TcRecord {
+    static constexpr bool sliced = false;
+    static constexpr uint32_t wq = 0;
+    static constexpr uint32_t aqk = 32768;
+    static constexpr uint32_t kb0 = 40960;
+    static constexpr uint32_t kb1 = 49152;
+    static constexpr uint32_t ut = 57344;
+    static constexpr uint32_t gamma = 73728;
+    static constexpr uint32_t used = gamma + 512;  // bytes the recurrence fetches
+    static constexpr uint32_t bytes = 74752;        // record stride (1024-aligned)
+};
+
+// Record of the value-sliced recurrence kernel (one CTA per 64 value columns): the same
+// tiles except U, which is token-major and split by value slice, placed so that each
+// slice's CTA fetches one contiguous run per chunk, [u1, u0) for slice 1 and
+// [wq, gamma) for slice 0:
+//   u1     U, values 64-127: [64 tokens][64] token-major.                         8 KB
+//   wq     [W ; Qg] as above (its panel 1 rows 64-127 followed by aqk form a 128-row A
+//          operand whose upper half only feeds accumulator rows never read).       32 KB
+//   aqk, kb0, kb1, gamma as above;  u0  U, values 0-63.                             8 KB
+struct TcRecordS {
+    static constexpr bool sliced = true;
     static constexpr uint32_t u1 = 0;
     static constexpr uint32_t wq = 8192;
     static constexpr uint32_t aqk = 40960;
@@ -141,8 +159,9 @@ struct TcRecord {
     static constexpr uint32_t kb1 = 57344;
     static constexpr uint32_t u0 = 65536;
     static constexpr uint32_t gamma = 73728;
-    static constexpr uint32_t bytes = 74752;  // record stride (1024-aligned)
+    static constexpr uint32_t bytes = 74752;
 };
+static_assert(TcRecordS::bytes == TcRecord::bytes, "both record forms share the workspace stride");
 
 // The bf16 tensor-core path serves K = V = 128; other bf16 shapes and fp32 take the
 // exact CUDA-core path.

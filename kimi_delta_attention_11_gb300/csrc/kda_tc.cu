@@ -25,23 +25,23 @@
 //   The results form one record per (chunk, head) (TcRecord), written as tensor-core
 //   operand images.
 //
-// kda_h_o_tc: one CTA (8 epilogue warps + 1 issuer warp) per (sequence, head, 64-column
-//   slice of V): the ordered chunk recurrence (Eq. (8)) fused with the output (Eq. (9)).
-//   The state slice lives in fp32 registers (thread (d, half) owns 32 columns of key row
-//   d) and is written as a bf16 operand tile each chunk.  Per chunk:
-//     MMA1  D1 = [W ; Qg] S                              (M 128, N 64, K 128)
-//     ep1   V_new = U - W S                               (D1 rows 0-63)
-//     MMA3  D3 = K_bar^T V_new                            (M 128 keys, N 64, K 64)
-//     MMA2  D1 += [Qg rows ; Aqk] V_new                   (rows 64-127: O = Qg S + Aqk V_new)
-//     ep2   S = Diag(gamma^C) S + D3.
-//   MMA3 is issued before MMA2 so that the state update, the only step the next chunk
-//   waits for, does not wait for the output product; D1 alternates between two TMEM
-//   buffers and each chunk's output rows are read while the next chunk's MMA1 runs.
-//   An issuer warp issues the record copies and every MMA and meets the epilogue warps at
-//   named barriers.  Records run through a ring of three stages, one bulk copy each, so
-//   each copy has two chunk steps to arrive.  Every tcgen05 product here reads both
-//   operands from shared memory, whose bandwidth (128 B per cycle) bounds it: the
-//   chained products are kept to the two that the method needs.
+// kda_h_o_tc: the ordered chunk recurrence (Eq. (8)) fused with the output (Eq. (9)), one
+//   CTA per (sequence, head) with all 128 value columns, in transposed form: the state
+//   S^T (bf16 copy) and V_new^T live in tensor memory as A operands, one lane per value
+//   column, so no shared-memory tile or proxy fence sits in the chain.  Per chunk:
+//     MMA1  D1 = S^T [W ; Qg]^T                          (M 128 values, N 128, K 128 keys)
+//     ep1   V_new^T = U^T - (W S)^T  -> tensor memory     (D1 columns 0-63)
+//     MMA3  D3 = V_new^T K_bar                            (N 128 keys, K 64 tokens)
+//     MMA2  D1[64:128] += V_new^T Aqk^T                   (O^T = (Qg S)^T + (Aqk V_new)^T)
+//     ep2   S^T = S^T Diag(gamma^C) + D3  -> tensor memory.
+//   Eight warps hold the fp32 state (lane = value column, half the keys each); four more
+//   warps read the output rows, so that reading them (which waits while the next chunk's
+//   product runs) stays off the chain; one warp issues copies and products.
+// sliced::kda_h_o_sliced_tc: the same recurrence untransposed with operands in shared
+//   memory, one CTA per 64-column value slice: faster when the chains are few.
+//   Every tcgen05 product here is bound by a fixed cost per K=16 step (about 90 cycles
+//   from shared memory, 105 with A in tensor memory, for N <= 128), so the chain keeps
+//   its products to the three the method needs.
 #include <mutex>
 
 #include "kda_internal.cuh"
@@ -144,7 +144,8 @@ struct IntraMap {
     static constexpr uint32_t XB = MISC;                 // X20, X31, X30, scratch [4][16][kBs]
     static constexpr uint32_t AIA = RB + 16384;          // (I + L)^{-1} bf16 [128][64]
     // after the W/U MMA
-    static constexpr uint32_t WST = KT, UST = VT;        // W, U staging (token-major)
+    static constexpr uint32_t WST = KT;                  // W staging (token-major)
+    static constexpr uint32_t UTS = VT;                  // U (token-major) or U^T staging
 };
 constexpr size_t kIntraSmem = IntraMap::END + 1024;  // + alignment slack
 // Row strides (floats) of the solve's fp32 tiles, chosen so that the fragment loads of
@@ -156,7 +157,9 @@ static_assert(4 * 16 * kBs * 4 <= IntraMap::END - IntraMap::MISC, "X blocks over
 
 // kOpts: the in-kernel gate activation / q-k normalisation are compiled in (a separate
 // instantiation, so the plain kernel carries none of their code or registers).
-template <bool kOpts>
+// Rec: the record form (TcRecord for the per-chain recurrence kernel, TcRecordS for the
+// value-sliced one).
+template <bool kOpts, typename Rec>
 __global__ void __launch_bounds__(kIntraThreads, 2)
 kda_intra_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
@@ -189,7 +192,7 @@ kda_intra_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     }
     const int4 ent = cx.chunk(c);
     const int t0 = ent.y, len = ent.z;
-    uint8_t* rec = records + ((size_t)slot * H + h) * TcRecord::bytes;
+    uint8_t* rec = records + ((size_t)slot * H + h) * Rec::bytes;
 
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -294,7 +297,7 @@ kda_intra_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             if (tid < 128) {
 #pragma unroll
                 for (int b = 0; b < 4; ++b) P0[b * 128 + d] = exp2f(gr[b]);
-                reinterpret_cast<float*>(rec + TcRecord::gamma)[d] = exp2f(gr[4]);
+                reinterpret_cast<float*>(rec + Rec::gamma)[d] = exp2f(gr[4]);
             } else {
 #pragma unroll
                 for (int b = 1; b < 4; ++b)
@@ -349,8 +352,8 @@ kda_intra_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                     qg[m] = qs[m] * p0[m];
                 }
                 sts128(sm, a, pack8(qs));
-                *reinterpret_cast<uint4*>(rec + TcRecord::wq + P * 16384 + 8192 +
-                                          sw128_chunk(i, cc)) = pack8(qg);
+                *reinterpret_cast<uint4*>(rec + Rec::wq + P * 16384 + 8192 +
+                                          sw128_chunk(i, cc)) = pack8(qg);  // rows 64-127
             }
             // key: relation B row, D_beta K+ (in place), key factor rows, K_bar
             {
@@ -368,7 +371,7 @@ kda_intra_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 }
                 sts128(sm, M::RB + (grp * 2 + P) * 8192 + sw128_chunk(32 + ii, cc), pack8(kp));
                 sts128(sm, a, pack8(kpl));
-                *reinterpret_cast<uint4*>(rec + (P ? TcRecord::kb1 : TcRecord::kb0) +
+                *reinterpret_cast<uint4*>(rec + (P ? Rec::kb1 : Rec::kb0) +
                                           sw128_chunk(i, cc)) = pack8(kb);
                 // round 0 of relation A: R_0 (rows 0-63) and R_1 (rows 64-127)
                 const uint32_t ra = M::RA + P * 16384;
@@ -621,17 +624,32 @@ kda_intra_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         __syncthreads();
     }
 
-    // [W | U] = (I+L)^{-1} [D_beta K+ | D_beta V]: M 128 (tokens, 64 used), N 256, K 64;
-    // B is the token-major k|v tiles (4 atoms of 64 columns, 8 KB apart).  The same thread
-    // then stores Aqk to the record, overlapping the product.
+    // W = (I+L)^{-1} D_beta K+ (M 128 tokens, 64 used; K 64) with B the token-major k
+    // tile rescaled in place (2 atoms, 8 KB apart), and U = (I+L)^{-1} D_beta V:
+    //  - sliced record: one N 256 product over the k | v tiles -> TMEM columns 0-255;
+    //  - per-chain record: U^T = (D_beta V)^T ((I+L)^{-1})^T instead, M 128 values (A = the
+    //    token-major v tile read as MN-major), N 64 tokens (B = (I+L)^{-1} itself, K-major)
+    //    -> columns 128-191, so the recurrence reads U^T rows.
+    // The same thread then stores Aqk to the record, overlapping the products.
     if (tid == 0) {
         tc_fence_after();
-        const uint32_t idesc = idesc_bf16(128, 256, false, true);
-        for (int kk = 0; kk < 4; ++kk)
-            mma_bf16(tmem, desc_sw128(sb + M::AIA + kk * 32),
-                     desc_sw128_mn(sb + M::KT + kk * 2048, 8192, 1024), idesc, kk > 0 ? 1u : 0u);
+        if constexpr (Rec::sliced) {
+            const uint32_t idesc = idesc_bf16(128, 256, false, true);
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16(tmem, desc_sw128(sb + M::AIA + kk * 32),
+                         desc_sw128_mn(sb + M::KT + kk * 2048, 8192, 1024), idesc, kk > 0 ? 1u : 0u);
+        } else {
+            const uint32_t id_w = idesc_bf16(128, 128, false, true);
+            const uint32_t id_u = idesc_bf16(128, 64, true, false);
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16(tmem, desc_sw128(sb + M::AIA + kk * 32),
+                         desc_sw128_mn(sb + M::KT + kk * 2048, 8192, 1024), id_w, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16(tmem + 128, desc_sw128_mn(sb + M::VT + kk * 2048, 8192, 1024),
+                         desc_sw128(sb + M::AIA + kk * 32), id_u, kk > 0 ? 1u : 0u);
+        }
         mma_commit(&bar_wu);
-        bulk_store(rec + TcRecord::aqk, sm + M::AQS, 8192);
+        bulk_store(rec + Rec::aqk, sm + M::AQS, 8192);
         bulk_commit();
     }
     mbar_wait_abortable(&bar_wu, 0, status, abort_flag);
@@ -639,11 +657,13 @@ kda_intra_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     __syncthreads();
     if (*abort_flag) goto teardown;
 
-    // W rows (warps 0,1) and U rows (warps 4,5) into token-major staging tiles, then to
-    // the record by bulk copies (whole lines, where per-thread row stores would not be)
-    if (warp == 0 || warp == 1 || warp == 4 || warp == 5) {
+    // W rows (warps 0,1; lane = token, 128 keys) into the token-major staging tile of the
+    // [W ; Qg] panels.  U: token-major rows (warps 4,5, sliced record) or U^T rows (warps
+    // 4-7; lane = value, 64 tokens) into a K-major [128][64] tile.  All go to the record by
+    // bulk copies (whole lines, where per-thread row stores would not be).
+    if (warp == 0 || warp == 1 || (Rec::sliced && (warp == 4 || warp == 5))) {
         const int r = (warp & 1) * 32 + lane;
-        const uint32_t dst = warp < 4 ? M::WST : M::UST;
+        const uint32_t dst = warp < 4 ? M::WST : M::UTS;
         const uint32_t col0 = warp < 4 ? 0 : 128;
         for (int cb = 0; cb < 4; ++cb) {
             float v[32];
@@ -656,15 +676,32 @@ kda_intra_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 sts128(sm, dst + (cb >> 1) * 8192 + sw128_chunk(r, (cb & 1) * 4 + qd), pack8(f));
             }
         }
+    } else if (!Rec::sliced && warp >= 4) {
+        const int r = (warp & 3) * 32 + lane;
+        for (int cb = 0; cb < 2; ++cb) {
+            float v[32];
+            tmem_ld32(tmem_addr(tmem, warp, 128 + 32 * cb), v);
+#pragma unroll
+            for (int qd = 0; qd < 4; ++qd) {
+                float f[8];
+#pragma unroll
+                for (int m = 0; m < 8; ++m) f[m] = v[qd * 8 + m];
+                sts128(sm, M::UTS + sw128_chunk(r, cb * 4 + qd), pack8(f));
+            }
+        }
     }
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     if (tid == 0) {
-        bulk_store(rec + TcRecord::wq, sm + M::WST, 8192);
-        bulk_store(rec + TcRecord::wq + 16384, sm + M::WST + 8192, 8192);
-        bulk_store(rec + TcRecord::u0, sm + M::UST, 8192);
-        bulk_store(rec + TcRecord::u1, sm + M::UST + 8192, 8192);
+        bulk_store(rec + Rec::wq, sm + M::WST, 8192);
+        bulk_store(rec + Rec::wq + 16384, sm + M::WST + 8192, 8192);
+        if constexpr (Rec::sliced) {
+            bulk_store(rec + TcRecordS::u0, sm + M::UTS, 8192);
+            bulk_store(rec + TcRecordS::u1, sm + M::UTS + 8192, 8192);
+        } else {
+            bulk_store(rec + TcRecord::ut, sm + M::UTS, 16384);
+        }
         bulk_commit();
         // only the shared-memory sources must outlive the copies; the stores themselves
         // are complete for any later kernel on the stream
@@ -680,6 +717,285 @@ teardown:
 // ---------------------------------------------------------------------------
 // recurrence + output kernel
 // ---------------------------------------------------------------------------
+
+constexpr int kEpiWarps = 8;              // warp w: TMEM lanes 32 (w % 4).. = value columns,
+                                          // half w / 4 of the keys / tokens
+constexpr int kIssuerWarp = kEpiWarps;    // record copies and MMA issue
+constexpr int kOutWarp0 = kEpiWarps + 1;  // 4 output warps (one per TMEM lane quadrant)
+constexpr int kHoThreads = (kEpiWarps + 5) * 32;
+constexpr uint32_t kChainThreads = (kEpiWarps + 1) * 32;  // named-barrier participants
+constexpr int kStages = 3;                // record ring depth: copies run 2 chunk steps ahead
+constexpr uint32_t kStage = TcRecord::bytes;
+// named barriers between the epilogue warps and the issuer warp
+constexpr uint32_t kBarVnew = 1;          // V_new^T written to tensor memory
+constexpr uint32_t kBarState = 2;         // S^T (bf16 operand) written, D3 / D1 read
+// tensor-memory columns (512 allocated: one CTA per SM)
+constexpr uint32_t kColD1 = 0;            // 2 x 128: [(W S)^T | O^T] per chunk, alternating
+constexpr uint32_t kColD3 = 256;          // 128: (K_bar^T V_new)^T
+constexpr uint32_t kColS = 384;           // 64: S^T as bf16 A operand (128 keys)
+constexpr uint32_t kColVn = 448;          // 32: V_new^T as bf16 A operand (64 tokens)
+constexpr size_t kHoSmem = kStages * kStage + 1024;
+static_assert(kHoSmem <= 232448, "recurrence kernel exceeds the shared-memory limit");
+static_assert(TcRecord::used <= kStage && TcRecord::kb1 == TcRecord::kb0 + 8192,
+              "record layout assumed by the recurrence kernel");
+
+// Whole warp: 16 consecutive 32-bit columns of the thread's own TMEM lane, then waits for
+// the stores to complete.
+__device__ __forceinline__ void tmem_st16_wait(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16};\n\t"
+        "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+
+__global__ void __launch_bounds__(kHoThreads, 1)
+kda_h_o_tc(const uint8_t* __restrict__ records, ChunkIndex cx, long long max_chunks, RangeArgs ra,
+           const float* __restrict__ s0, __nv_bfloat16* __restrict__ o, float* __restrict__ sN,
+           int H, int* __restrict__ status) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ uint64_t full[kStages], bar_m1, bar_m3, bar_m2[2], bar_out[2];
+    __shared__ uint32_t tmem_base;
+    __shared__ int s_abort;
+
+    const int h = blockIdx.x % H;
+    const int n = blockIdx.x / H;
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    const uint32_t sb = smem_u32(sm);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int2 sq = cx.seq(n);
+    int seq_chunks = sq.y;
+    if ((long long)sq.x + seq_chunks > max_chunks) {  // inconsistent cu_seqlens: stop rather than overrun
+        if (tid == 0) atomicCAS(status, 0, (int)KDA_ERR_INVALID_ARG);
+        seq_chunks = (int)(max_chunks > sq.x ? max_chunks - sq.x : 0);
+    }
+    // this launch runs chunks lo <= j < hi of the sequence (all of them, or one range of a
+    // pipelined call); the state comes from initial_state (or zeros) at j = 0, else from
+    // the carry buffer, and goes to final_state after the sequence's last chunk, else to
+    // the carry buffer
+    const int lo = ra.span ? ra.j0 : 0;
+    const int hi = ra.span ? min(ra.j0 + ra.span, seq_chunks) : seq_chunks;
+    if (lo >= hi && !(lo == 0 && seq_chunks == 0)) return;  // nothing of this sequence here
+    const int nch = hi > lo ? hi - lo : 0;
+    const long long first = (long long)sq.x + lo;            // global index of chunk lo
+    const long long slot0 = ra.span ? (long long)n * ra.span : first;
+    const float* s_in = lo == 0 ? s0 : ra.carry;
+    float* s_out = hi == seq_chunks ? sN : ra.carry;
+    auto rec_of = [&](int ci) {
+        return records + ((size_t)(slot0 + ci) * H + h) * TcRecord::bytes;
+    };
+
+    if (warp == 0) tmem_alloc(&tmem_base, 512);
+    if (tid == 0) {
+        s_abort = 0;
+        for (int i = 0; i < kStages; ++i) mbar_init(&full[i], 1);
+        mbar_init(&bar_m1, 1);
+        mbar_init(&bar_m3, 1);
+        mbar_init(&bar_m2[0], 1);
+        mbar_init(&bar_m2[1], 1);
+        mbar_init(&bar_out[0], 4 * 32);
+        mbar_init(&bar_out[1], 4 * 32);
+        fence_barrier_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base;
+    volatile int* abort_flag = &s_abort;
+
+    if (warp >= kOutWarp0) {
+        // ---- output warps: O^T of chunk ci from D1 columns 64-127 (lane = value v, all 64
+        // query rows), read while the chain goes on, then the D1 buffer is handed back ----
+        // a warp reaches only the TMEM lanes of its own sub-partition (warp % 4)
+        const int qd = warp & 3, v = qd * 32 + lane;
+        for (int ci = 0; ci < nch; ++ci) {
+            if (!__all_sync(0xffffffffu, mbar_wait_abortable(&bar_m2[ci & 1], (ci >> 1) & 1, status,
+                                                             abort_flag)))
+                break;
+            tc_fence_after();
+            const int4 ent = cx.chunk(first + ci);
+            __nv_bfloat16* dst = o + ((size_t)ent.y * H + h) * 128 + v;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                float ov[32];
+                tmem_ld32(tmem_addr(tmem + kColD1 + 128 * (ci & 1) + 64 + 32 * hh, qd, 0), ov);
+#pragma unroll
+                for (int x = 0; x < 32; ++x) {
+                    const int i = 32 * hh + x;
+                    if (i < ent.z) dst[(size_t)i * H * 128] = __float2bfloat16_rn(ov[x]);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&bar_out[ci & 1]);
+        }
+    } else if (warp == kIssuerWarp) {
+        // ---- issuer warp: record copies and every MMA (lane 0 issues).  The whole warp
+        // runs the loop so that its named-barrier syncs are warp-uniform; every exit
+        // decision is made uniform with a warp vote. ----
+        auto load = [&](int ci) {  // record of chunk ci into stage ci % kStages (lane 0)
+            const int sg = ci % kStages;
+            mbar_arrive_expect_tx(&full[sg], TcRecord::used);
+            bulk_load(sm + sg * kStage, rec_of(ci), TcRecord::used, &full[sg]);
+        };
+        if (lane == 0)
+            for (int ci = 0; ci < kStages && ci < nch; ++ci) load(ci);
+        __syncwarp();
+        const uint32_t id_1 = idesc_bf16(128, 128, false, false);  // D1 = S^T [W ; Qg]^T
+        const uint32_t id_3 = idesc_bf16(128, 128, false, true);   // D3 = V_new^T K_bar
+        const uint32_t id_2 = idesc_bf16(128, 64, false, false);   // O^T += V_new^T Aqk^T
+        for (int ci = 0; ci < nch; ++ci) {
+            const int sg = ci % kStages;
+            const uint32_t stb = sb + sg * kStage;
+            const uint32_t D1 = tmem + kColD1 + 128 * (ci & 1);
+            bool ok = mbar_wait_abortable(&full[sg], (ci / kStages) & 1, status, abort_flag);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            named_bar_sync(kBarState, kChainThreads);  // S_ci^T in tensor memory
+            if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+            if (ci >= 2) {  // D1 buffer of chunk ci-2 read by the output warps
+                ok = mbar_wait_abortable(&bar_out[ci & 1], ((ci - 2) >> 1) & 1, status, abort_flag);
+                if (!__all_sync(0xffffffffu, ok)) break;
+            }
+            if (lane == 0) {
+                tc_fence_after();
+                // MMA1: D1 = S^T [W ; Qg]^T   (K = 128 keys: A 8 columns per step, B two
+                // K-major panels)
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_bf16_ta(D1, tmem + kColS + 8 * ks,
+                                desc_sw128(stb + TcRecord::wq + (ks >> 2) * 16384 + (ks & 3) * 32),
+                                id_1, ks > 0 ? 1u : 0u);
+                mma_commit(&bar_m1);
+            }
+            __syncwarp();
+            // refill the stage chunk ci-1 used: its MMA2 precedes this MMA1 on the pipe
+            if (ci >= 1 && ci - 1 + kStages < nch) {
+                ok = mbar_wait_abortable(&bar_m2[(ci - 1) & 1], ((ci - 1) >> 1) & 1, status, abort_flag);
+                if (!__all_sync(0xffffffffu, ok)) break;
+                if (lane == 0) load(ci - 1 + kStages);
+                __syncwarp();
+            }
+            named_bar_sync(kBarVnew, kChainThreads);  // V_new^T in tensor memory
+            if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+            if (lane == 0) {
+                tc_fence_after();
+                // MMA3 first (it feeds the state): D3 = V_new^T K_bar (K = 64 tokens; K_bar
+                // token-major: MN-major B, 2 atoms 8 KB apart)
+                const uint64_t dKB = desc_sw128_mn(stb + TcRecord::kb0, 8192, 1024);
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16_ta(tmem + kColD3, tmem + kColVn + 8 * kk,
+                                dKB + (uint64_t)((kk * 2048) >> 4), id_3, kk > 0 ? 1u : 0u);
+                mma_commit(&bar_m3);
+                // MMA2: D1 columns 64-127 += V_new^T Aqk^T  (O^T = (Qg S)^T + (Aqk V_new)^T)
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16_ta(D1 + 64, tmem + kColVn + 8 * kk,
+                                desc_sw128(stb + TcRecord::aqk + kk * 32), id_2, 1u);
+                mma_commit(&bar_m2[ci & 1]);
+            }
+            __syncwarp();
+        }
+    } else {
+        // ---- epilogue warps: thread (v, half) owns value column v (TMEM lane) and keys
+        // 64 half .. 64 half + 63 of the state, fp32 ----
+        const int qd = warp & 3, half = warp >> 2, v = qd * 32 + lane;
+        const size_t st_base = ((size_t)n * H + h) * 128 * 128 + (size_t)(64 * half) * 128 + v;
+        float S[64];
+#pragma unroll
+        for (int x = 0; x < 64; ++x) S[x] = s_in ? s_in[st_base + (size_t)x * 128] : 0.f;
+        // S^T as bf16 operand columns (2 keys per column) of this thread's lane
+        auto write_state = [&]() {
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int m = 0; m < 16; ++m) pk[m] = pack_bf16x2(S[32 * hh + 2 * m], S[32 * hh + 2 * m + 1]);
+                tmem_st16_wait(tmem_addr(tmem + kColS + 32 * half + 16 * hh, qd, 0), pk);
+            }
+            tc_fence_before();
+            named_bar_arrive(kBarState, kChainThreads);
+        };
+        write_state();
+        for (int ci = 0; ci < nch; ++ci) {
+            const int sg = ci % kStages;
+            const uint32_t D1 = tmem + kColD1 + 128 * (ci & 1);
+            const uint8_t* st = sm + sg * kStage;
+            if (!__all_sync(0xffffffffu,
+                            mbar_wait_abortable(&full[sg], (ci / kStages) & 1, status, abort_flag)))
+                break;
+            // U^T is fetched before the product it combines with completes
+            uint4 ur[4];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) ur[q4] = lds128(st, TcRecord::ut + sw128_chunk(v, 4 * half + q4));
+            if (!__all_sync(0xffffffffu, mbar_wait_abortable(&bar_m1, ci & 1, status, abort_flag)))
+                break;
+            tc_fence_after();
+            {
+                // ep1: V_new^T[v][t] = U^T[v][t] - (W S)^T[v][t], tokens 32 half .. + 31
+                float ws[32];
+                tmem_ld32(tmem_addr(D1 + 32 * half, qd, 0), ws);
+                uint32_t pk[16];
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    float uf[8];
+                    unpack8(ur[q4], uf);
+#pragma unroll
+                    for (int m = 0; m < 4; ++m)
+                        pk[4 * q4 + m] = pack_bf16x2(uf[2 * m] - ws[8 * q4 + 2 * m],
+                                                     uf[2 * m + 1] - ws[8 * q4 + 2 * m + 1]);
+                }
+                tmem_st16_wait(tmem_addr(tmem + kColVn + 16 * half, qd, 0), pk);
+                tc_fence_before();
+                named_bar_arrive(kBarVnew, kChainThreads);
+            }
+            if (!__all_sync(0xffffffffu, mbar_wait_abortable(&bar_m3, ci & 1, status, abort_flag)))
+                break;
+            tc_fence_after();
+            // ep2: S[v][key] = gamma[key] S[v][key] + D3[v][key], keys 64 half .. + 63
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                float upd[32];
+                tmem_ld32(tmem_addr(tmem + kColD3 + 64 * half + 32 * hh, qd, 0), upd);
+                const float4* gp =
+                    reinterpret_cast<const float4*>(st + TcRecord::gamma) + 16 * half + 8 * hh;
+#pragma unroll
+                for (int x = 0; x < 8; ++x) {
+                    const float4 g4 = gp[x];
+                    float* sx = S + 32 * hh + 4 * x;
+                    sx[0] = fmaf(g4.x, sx[0], upd[4 * x]);
+                    sx[1] = fmaf(g4.y, sx[1], upd[4 * x + 1]);
+                    sx[2] = fmaf(g4.z, sx[2], upd[4 * x + 2]);
+                    sx[3] = fmaf(g4.w, sx[3], upd[4 * x + 3]);
+                }
+            }
+            write_state();  // S_{ci+1}; releases the issuer for the next chunk
+        }
+        // after an expired wait, release the issuer from whichever named barrier it may
+        // be waiting at (surplus arrivals are harmless: the CTA ends)
+        if (__any_sync(0xffffffffu, *abort_flag != 0)) {
+            named_bar_arrive(kBarState, kChainThreads);
+            named_bar_arrive(kBarVnew, kChainThreads);
+        }
+        if (s_out && !*abort_flag) {
+#pragma unroll
+            for (int x = 0; x < 64; ++x) s_out[st_base + (size_t)x * 128] = S[x];
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+// Value-sliced recurrence: one CTA (8 epilogue warps + 1 issuer warp) per (sequence,
+// head, 64-column slice of V), untransposed products with both operands in shared
+// memory.  Used when the chains are few (two CTAs per chain fill the SMs and the
+// shorter chained products win); see kda_h_o_tc for the per-chain form.
+//   MMA1  D1 = [W ; Qg] S                              (M 128, N 64, K 128)
+//   ep1   V_new = U - W S                               (D1 rows 0-63)
+//   MMA3  D3 = K_bar^T V_new                            (M 128 keys, N 64, K 64)
+//   MMA2  D1 += [Qg rows ; Aqk] V_new                   (rows 64-127: O = Qg S + Aqk V_new)
+//   ep2   S = Diag(gamma^C) S + D3.
+namespace sliced {
 
 constexpr int kVT = 64;                   // value columns per CTA
 constexpr int kEpiWarps = 8;              // warp w: TMEM lanes 32 (w % 4).., value columns
@@ -699,12 +1015,12 @@ struct HoMap {
 };
 constexpr size_t kHoSmem = HoMap::END + 1024;
 static_assert(kHoSmem <= 232448, "recurrence kernel exceeds the shared-memory limit");
-static_assert(TcRecord::u1 == 0 && TcRecord::u0 == kStage && TcRecord::gamma == kStage + 8192 &&
-                  TcRecord::aqk == TcRecord::wq + 32768 && TcRecord::kb1 == TcRecord::kb0 + 8192,
+static_assert(TcRecordS::u1 == 0 && TcRecordS::u0 == kStage && TcRecordS::gamma == kStage + 8192 &&
+                  TcRecordS::aqk == TcRecordS::wq + 32768 && TcRecordS::kb1 == TcRecordS::kb0 + 8192,
               "record layout assumed by the recurrence kernel");
 
 __global__ void __launch_bounds__(kHoThreads, 1)
-kda_h_o_tc(const uint8_t* __restrict__ records, ChunkIndex cx, long long max_chunks, RangeArgs ra,
+kda_h_o_sliced_tc(const uint8_t* __restrict__ records, ChunkIndex cx, long long max_chunks, RangeArgs ra,
            const float* __restrict__ s0, __nv_bfloat16* __restrict__ o, float* __restrict__ sN,
            int H, int* __restrict__ status) {
     using M = HoMap;
@@ -739,12 +1055,12 @@ kda_h_o_tc(const uint8_t* __restrict__ records, ChunkIndex cx, long long max_chu
     const float* s_in = lo == 0 ? s0 : ra.carry;
     float* s_out = hi == seq_chunks ? sN : ra.carry;
     auto rec_of = [&](int ci) {
-        return records + ((size_t)(slot0 + ci) * H + h) * TcRecord::bytes;
+        return records + ((size_t)(slot0 + ci) * H + h) * TcRecordS::bytes;
     };
     // slice s copies record bytes [cs, cs + kStage): stage offset = record offset - cs
-    const uint32_t cs = slice ? TcRecord::u1 : TcRecord::wq;
-    const uint32_t WQ = TcRecord::wq - cs, AQK = TcRecord::aqk - cs, KB = TcRecord::kb0 - cs;
-    const uint32_t UO = (slice ? TcRecord::u1 : TcRecord::u0) - cs;
+    const uint32_t cs = slice ? TcRecordS::u1 : TcRecordS::wq;
+    const uint32_t WQ = TcRecordS::wq - cs, AQK = TcRecordS::aqk - cs, KB = TcRecordS::kb0 - cs;
+    const uint32_t UO = (slice ? TcRecordS::u1 : TcRecordS::u0) - cs;
 
     if (warp == 0) tmem_alloc(&tmem_base, 256);
     if (tid == 0) {
@@ -880,7 +1196,7 @@ kda_h_o_tc(const uint8_t* __restrict__ records, ChunkIndex cx, long long max_chu
         };
         // gamma^C of the next chunks, fetched two chunk steps ahead
         auto gamma_of = [&](int ci) {
-            return ci < nch ? reinterpret_cast<const float*>(rec_of(ci) + TcRecord::gamma)[d] : 0.f;
+            return ci < nch ? reinterpret_cast<const float*>(rec_of(ci) + TcRecordS::gamma)[d] : 0.f;
         };
         float gam0 = gamma_of(0), gam1 = gamma_of(1);
         write_state();
@@ -951,6 +1267,8 @@ kda_h_o_tc(const uint8_t* __restrict__ records, ChunkIndex cx, long long max_chu
     if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
+}  // namespace sliced
+
 }  // namespace
 
 namespace {
@@ -1009,15 +1327,25 @@ cudaError_t launch_tc(const void* q, const void* k, const void* v, const float* 
             !make_tmap_2d(&tv, v, true, inner, rows, inner * 2, 64, 64, true) ||
             !make_tmap_2d(&tg, g, false, inner, rows, inner * 4, 128, 64, false))
             return cudaErrorInvalidValue;
-        cudaFuncSetAttribute(kda_intra_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kIntraSmem);
-        cudaFuncSetAttribute(kda_intra_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kIntraSmem);
     }
-    cudaFuncSetAttribute(kda_h_o_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kHoSmem);
+    // Recurrence form: value-sliced (two CTAs per chain, shorter chained products) while
+    // two CTAs per chain fit in one wave of SMs, else one CTA per chain (no work repeated
+    // per slice).  The intra-chunk kernel writes the record form that kernel reads.
+    int dev = 0, sms = 0;
+    if (cudaError_t e = cudaGetDevice(&dev)) return e;
+    if (cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) return e;
+    const bool sliced = 2ll * L.N * H <= sms;
+    const bool opts = ga.mode != 0 || ga.qk_l2norm;
+    auto* intra = sliced ? (opts ? kda_intra_tc<true, TcRecordS> : kda_intra_tc<false, TcRecordS>)
+                         : (opts ? kda_intra_tc<true, TcRecord> : kda_intra_tc<false, TcRecord>);
+    auto* ho = sliced ? sliced::kda_h_o_sliced_tc : kda_h_o_tc;
+    const unsigned ho_blocks = (unsigned)L.N * H * (sliced ? 2 : 1);
+    const unsigned ho_threads = sliced ? sliced::kHoThreads : kHoThreads;
+    const size_t ho_smem = sliced ? sliced::kHoSmem : kHoSmem;
+    if (L.max_chunks > 0)
+        cudaFuncSetAttribute(intra, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kIntraSmem);
+    cudaFuncSetAttribute(ho, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ho_smem);
     __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(o);
-    auto* intra = (ga.mode != 0 || ga.qk_l2norm) ? kda_intra_tc<true> : kda_intra_tc<false>;
-    const unsigned ho_blocks = (unsigned)L.N * H * 2;
 
     // Whole-problem schedule: one launch of each kernel (and the only one with per-kernel
     // timing events).
@@ -1030,8 +1358,8 @@ cudaError_t launch_tc(const void* q, const void* k, const void* v, const float* 
         }
         if (!record_event(ev, 0, s)) return cudaErrorInvalidResourceHandle;
         if (L.N > 0) {
-            kda_h_o_tc<<<ho_blocks, kHoThreads, kHoSmem, s>>>(records, cx, L.max_chunks, RangeArgs{},
-                                                              s0, ob, sN, H, status);
+            ho<<<ho_blocks, ho_threads, ho_smem, s>>>(records, cx, L.max_chunks, RangeArgs{}, s0, ob,
+                                                      sN, H, status);
             if (cudaError_t e = cudaGetLastError()) return e;
         }
         if (!record_event(ev, 1, s)) return cudaErrorInvalidResourceHandle;
@@ -1042,8 +1370,6 @@ cudaError_t launch_tc(const void* q, const void* k, const void* v, const float* 
     // recurrence on the side stream once range r's records exist and range r - 1's
     // recurrence has handed over the state; records live in a ring of L.ring range slots,
     // so intra of range r waits for the recurrence of range r - ring to have read them.
-    int dev = 0;
-    if (cudaError_t e = cudaGetDevice(&dev)) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_pipe_mu);
     PipeRes* P = nullptr;
@@ -1063,8 +1389,8 @@ cudaError_t launch_tc(const void* q, const void* k, const void* v, const float* 
         if (cudaError_t e = cudaGetLastError()) return e;
         if (cudaError_t e = cudaEventRecord(P->intra_done[sl], s)) return e;
         if (cudaError_t e = cudaStreamWaitEvent(P->side, P->intra_done[sl], 0)) return e;
-        kda_h_o_tc<<<ho_blocks, kHoThreads, kHoSmem, P->side>>>(rec, cx, L.max_chunks, ra, s0,
-                                                                 ob, sN, H, status);
+        ho<<<ho_blocks, ho_threads, ho_smem, P->side>>>(rec, cx, L.max_chunks, ra, s0, ob, sN, H,
+                                                          status);
         if (cudaError_t e = cudaGetLastError()) return e;
         if (cudaError_t e = cudaEventRecord(P->ho_done[sl], P->side)) return e;
     }

@@ -48,3 +48,17 @@ def test_umma_gemm_a_mn_major(kda, N, K):
     D = kda.selftest_umma(At.contiguous(), B, 3)
     ref = At.double().T @ B.double().T
     assert (D.double() - ref).abs().max().item() <= 1e-3 * max(1.0, ref.abs().max().item())
+
+
+@pytest.mark.parametrize("N", [16, 64, 128, 256])
+@pytest.mark.parametrize("K", [16, 64, 128])
+def test_umma_gemm_a_in_tmem(kda, N, K):
+    """A written to tensor memory with tcgen05.st (row m in lane m, two bf16 per 32-bit
+    column), B in shared memory: the operand form of the recurrence kernel's chained
+    products."""
+    g = torch.Generator(device="cpu").manual_seed(13 * N + K)
+    A = torch.randn((128, K), generator=g).to(torch.bfloat16).cuda()
+    B = torch.randn((N, K), generator=g).to(torch.bfloat16).cuda()
+    D = kda.selftest_umma(A, B, 4)
+    ref = A.double() @ B.double().T
+    assert (D.double() - ref).abs().max().item() <= 1e-3 * max(1.0, ref.abs().max().item())

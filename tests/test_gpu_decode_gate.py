@@ -111,10 +111,10 @@ def _activated(orc, gd, graw, q, k):
 
 
 @pytest.mark.parametrize("form", list(GATES))
-@pytest.mark.parametrize("path", ["tc_bf16", "simt_f32"])
+@pytest.mark.parametrize("path", ["tc_bf16", "tc_bf16_many_chains", "simt_f32"])
 def test_gate_activation_fwd(kda, orc, form, path):
-    dtype, K = (torch.bfloat16, 128) if path == "tc_bf16" else (torch.float32, 64)
-    B, T, H = 2, 150, 3
+    dtype, K = (torch.float32, 64) if path == "simt_f32" else (torch.bfloat16, 128)
+    B, T, H = (2, 150, 3) if path != "tc_bf16_many_chains" else (6, 90, 14)
     g = torch.Generator().manual_seed(5 + len(form) + K)
     q = torch.randn((B, T, H, K), generator=g).to(dtype)   # not normalised: the kernel does it
     k = torch.randn((B, T, H, K), generator=g).to(dtype)

@@ -158,6 +158,18 @@ def test_pipelined_schedule(kda, orc, shape):
     assert eo <= 2e-2 and ef <= 2e-2, (eo, ef)
 
 
+@pytest.mark.parametrize("shape", [(6, 200, 14, 0.2), (1, 130, 80, None)],
+                         ids=["84chains_init", "80chains"])
+def test_per_chain_recurrence_form(kda, orc, shape):
+    """With more chains than two CTAs per chain fit in one wave, the recurrence runs one CTA
+    per (sequence, head) on the transposed record form; it must agree with the oracle like
+    the value-sliced form the small cases use."""
+    B, T, H, init = shape
+    inp = make_inputs(custom(B=B, T=T, H=H, K=128, V=128, dtype=torch.bfloat16, init_std=init,
+                             seed=B + T + H), device="cuda")
+    check(kda, orc, inp)
+
+
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
 def test_split_call_resume(kda, dtype):
     inp = make_inputs(custom(B=2, T=300, H=2, K=128, V=128, dtype=dtype, init_std=0.1, seed=43),
