@@ -170,16 +170,16 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
-def ncu_traffic(kernel: str):
+def ncu_traffic(kernel: str, workload: str):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, if the summary
-    was taken on the current kernel source (else None)."""
+    was taken on this workload and on the current kernel source (else None)."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
     ent = d.get(kernel)
-    if not ent:
+    if not ent or ent.get("workload") != workload:
         return None
     src = os.path.join(ROOT, ent["source"])
     if not os.path.exists(src):
@@ -369,7 +369,11 @@ def run_ours(args, rank, world, local):
     tokens_all = alg["tokens"] * world
     value = tokens_all / (ms * 1e-3)
     tc = inp["dtype"] == torch.bfloat16 and K == 128 and V == 128
-    names = (["kda_chunk_index", "kda_intra_tc", "kda_h_o_tc"] if tc
+    # the recurrence runs value-sliced (two CTAs per chain) when 2 x chains fit the SMs
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    chains = (N if inp["cu_seqlens"] is not None else B) * H
+    ho_tc = "kda_h_o_sliced_tc" if 2 * chains <= sms else "kda_h_o_tc"
+    names = (["kda_chunk_index", "kda_intra_tc", ho_tc] if tc
              else ["kda_chunk_index", "kda_intra_simt", "kda_h_o_simt"])
     avg = [sum(s[j] for s in stage_ms) / args.steps for j in range(3)]
     dom = max(range(3), key=lambda j: avg[j])
@@ -388,7 +392,7 @@ def run_ours(args, rank, world, local):
         "roofline": {"bound": "hbm", "kernel": names[dom], "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": f"{peak_kind} hbm_gbs",
-                     "traffic": ncu_traffic(names[dom])},
+                     "traffic": ncu_traffic(names[dom], w.name)},
         "path_roofline": {"algorithmic_bytes": alg["bytes"], "achieved_GBps": path_achieved,
                           "frac_of_measured_hbm": path_achieved / peak,
                           "algorithmic_flops": alg["flops"]},
@@ -468,7 +472,8 @@ def run_decode(args, rank, world, local):
                    "l2": "flushed between timed steps (write of 4x L2)"},
         "roofline": {"bound": "hbm", "kernel": "kda_decode_kernel", "achieved": achieved,
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "peak_source": f"{peak_kind} hbm_gbs", "traffic": None,
+                     "peak_source": f"{peak_kind} hbm_gbs",
+                     "traffic": ncu_traffic("kda_decode", args.workload),
                      "bytes_per_step": step_bytes},
         "gpu_launches": args.steps, "clocks": clocks, "wall_s_timed": wall,
     }
