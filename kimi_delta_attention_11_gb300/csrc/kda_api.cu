@@ -4,10 +4,38 @@
 // intra-chunk stage and the state/output recurrence are launched on the caller's
 // stream with no host synchronisation and no allocation.
 #include <limits.h>
+#include <cstdlib>
+#include <cstring>
 
 #include "kda_internal.cuh"
 
 namespace kda {
+
+// Schedule request from the KDA_SCHEDULE environment variable ("two", "pipelined",
+// "fused"; anything else or unset: automatic).  A forced schedule that does not apply to
+// the sizes falls back to the automatic choice's next option (see make_layout).
+Schedule schedule_request() {
+    const char* e = std::getenv("KDA_SCHEDULE");
+    if (!e) return Schedule::kAuto;
+    if (!std::strcmp(e, "two")) return Schedule::kTwo;
+    if (!std::strcmp(e, "pipelined")) return Schedule::kPipelined;
+    if (!std::strcmp(e, "fused")) return Schedule::kFused;
+    return Schedule::kAuto;
+}
+
+// SM count of the current device, 0 without one (then no schedule depends on it).
+int current_sm_count() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return sms;
+}
 
 Layout make_layout(int B, int T, int H, int K, int V, int num_seqs, bool packed, kda_dtype dt) {
     Layout L;
@@ -24,6 +52,14 @@ Layout make_layout(int B, int T, int H, int K, int V, int num_seqs, bool packed,
                                            : align_up(SimtRecord::floats(K, V) * sizeof(float), 1024);
     L.total = L.inter_off + (size_t)L.max_chunks * H * L.inter_stride;
     L.fixed = use_tc_path(K, V, dt) && !packed;
+    const Schedule want = schedule_request();
+    const long long chains = (long long)B * H;
+    const int sms = L.fixed && L.max_chunks > 0 ? current_sm_count() : 0;
+    // Fused: the recurrences of few chains occupy few SMs for the whole call, so the
+    // records are produced on the other SMs while they run (one CTA per SM, both
+    // stages in one cooperative launch).  Automatic up to a third of the SMs.
+    const bool can_fuse = L.fixed && L.max_chunks > 0 && sms > 0 && 2 * chains <= sms;
+    const bool auto_fuse = can_fuse && 3 * chains <= sms;
     // Pipelining pays when the recurrence has few, long chains (its ordered chunk steps,
     // not the SM count, set its time): fixed-length input, at most 128 (sequence, head)
     // chains and at least 512 chunks per sequence (measured on GB300: a 6 % gain at
@@ -31,7 +67,13 @@ Layout make_layout(int B, int T, int H, int K, int V, int num_seqs, bool packed,
     // need a whole SM each, wait for the next range's intra-chunk CTAs to drain).
     // Ranges of 32 chunks; a ring of 3 ranges of records so the intra-chunk kernel can
     // run up to 2 ranges ahead.
-    if (use_tc_path(K, V, dt) && !packed && (long long)B * H <= 128 && nct >= kPipeMinChunks) {
+    const bool can_pipe = L.fixed && chains <= 128 && nct >= 2;
+    const bool auto_pipe = can_pipe && nct >= kPipeMinChunks;
+    if (want == Schedule::kFused ? can_fuse : (want == Schedule::kAuto && auto_fuse)) {
+        L.fused = true;
+        L.flags_off = align_up(L.total, 256);
+        L.total = L.flags_off + (size_t)L.max_chunks * H * sizeof(int);
+    } else if (want == Schedule::kPipelined ? can_pipe : (want == Schedule::kAuto && auto_pipe)) {
         L.span = 32;
         L.ranges = (int)((nct + L.span - 1) / L.span);
         L.ring = 3;
@@ -99,6 +141,7 @@ int kda_fwd_launch_count(int B, int T, int H, int K, int V, int num_seqs, int ch
     if (check_sizes(B, T, H, K, V, num_seqs, packed, chunk_size, dtype) != KDA_OK) return -1;
     const Layout L = make_layout(B, T, H, K, V, num_seqs, packed, dtype);
     const int index = L.fixed ? 0 : 1;
+    if (L.fused) return 1;
     if (L.span > 0) return index + 2 * L.ranges;
     return index + (L.max_chunks > 0 ? 1 : 0) + (L.N > 0 ? 1 : 0);
 }

@@ -13,6 +13,9 @@ namespace kda {
 constexpr int kChunk = 64;  // chunk size C: the production path fixes C = 64
 constexpr int kPipeMinChunks = 512;  // chunks per sequence from which calls are pipelined
 
+// Launch schedule of a call (see make_layout).
+enum class Schedule { kAuto, kTwo, kPipelined, kFused };
+
 // Byte layout of the caller's workspace.
 //   [0, 4)       int32 device status word (0 = ok, else a kda_status)
 //   [16, 20)     int32 number of chunks, written by the chunk-index kernel
@@ -39,6 +42,11 @@ struct Layout {
     // fixed-length input on the tensor-core path: chunk facts are arithmetic (ChunkIndex)
     // and no chunk-index kernel runs
     bool fixed = false;
+    // Fused schedule (tensor-core path, fixed-length input with few chains): one
+    // cooperative launch in which some CTAs run the recurrences and the rest produce the
+    // records, published through one flag word per (chunk, head) at flags_off.
+    bool fused = false;
+    size_t flags_off = 0;
 };
 
 // Where the kernels find a chunk's sequence, first token, length and index within its

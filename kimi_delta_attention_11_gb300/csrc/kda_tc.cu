@@ -155,47 +155,38 @@ static_assert(IntraMap::LF + 64 * kLs * 4 <= IntraMap::RA + 32768, "L tile overf
 static_assert(IntraMap::JB + 6 * 16 * kBs * 4 <= IntraMap::AIA, "J blocks overflow");
 static_assert(4 * 16 * kBs * 4 <= IntraMap::END - IntraMap::MISC, "X blocks overflow");
 
+// One chunk-head of the intra-chunk stage, run by one "lane" of kIntraThreads threads
+// (lane-local named barrier 1 + lid, lane-local mbarriers): the standalone kernel has one
+// lane per CTA; the fused kernel two per CTA, each working through many chunk-heads.
 // kOpts: the in-kernel gate activation / q-k normalisation are compiled in (a separate
 // instantiation, so the plain kernel carries none of their code or registers).
 // Rec: the record form (TcRecord for the per-chain recurrence kernel, TcRecordS for the
 // value-sliced one).
-template <bool kOpts, typename Rec>
-__global__ void __launch_bounds__(kIntraThreads, 2)
-kda_intra_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
-             const float* __restrict__ beta, float scale, GateArgs ga, int H, ChunkIndex cx,
-             long long max_chunks, RangeArgs ra, uint8_t* __restrict__ records,
-             int* __restrict__ status) {
+// `sm` is the lane's 1024-aligned shared-memory base, `tmem` its 256 tensor-memory
+// columns.  With `flag`, the record is published once complete: the bulk stores are
+// waited for, then *flag is set with release semantics (the recurrence CTA of the same
+// launch polls it).  Returns false after an expired wait.
+template <bool kOpts, typename Rec, int kLid>
+__device__ __forceinline__ bool intra_unit(const CUtensorMap* tmq, const CUtensorMap* tmk,
+                                           const CUtensorMap* tmv, const CUtensorMap* tmg,
+                                           const float* __restrict__ beta, float scale,
+                                           const GateArgs& ga, int H, const ChunkIndex& cx,
+                                           long long c, int h, uint8_t* __restrict__ rec,
+                                           int* __restrict__ prev_flag, bool publish,
+                                           uint8_t* sm, uint32_t tmem, int lid_arg,
+                                           int tid, uint32_t k, int* __restrict__ status) {
+    // kLid >= 0: the lane index is a constant (the standalone kernel); -1: lid_arg
+    const int lid = kLid >= 0 ? kLid : lid_arg;
     using M = IntraMap;
-    extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t bar_tma, bar_rel, bar_wu;
-    __shared__ uint32_t tmem_base;
-    __shared__ int s_abort;
-
-    const long long blk = blockIdx.x;
-    const int h = (int)(blk % H);
-    long long c, slot;
-    if (ra.span == 0) {
-        // whole problem: chunks from the last to the first, so that the records of early
-        // chunks, which the recurrence reads first, are the most recently written
-        c = max_chunks - 1 - blk / H;
-        if (c >= cx.num_chunks(max_chunks)) return;
-        slot = c;
-    } else {
-        // chunks j0 <= j < j0 + span of every sequence (j = index within the sequence)
-        const long long rest = blk / H;
-        const int jj = (int)(rest % ra.span), n = (int)(rest / ra.span);
-        const int2 sq = cx.seq(n);
-        if (ra.j0 + jj >= sq.y) return;
-        c = sq.x + ra.j0 + jj;
-        slot = (long long)n * ra.span + jj;
-    }
+    __shared__ uint64_t s_bar_tma[2], s_bar_rel[2], s_bar_wu[2];
+    __shared__ int s_abort_l[2];
+    uint64_t& bar_tma = s_bar_tma[lid];
+    uint64_t& bar_rel = s_bar_rel[lid];
+    uint64_t& bar_wu = s_bar_wu[lid];
+    const uint32_t lane_bar = 1 + (uint32_t)lid;
+    auto lane_sync = [&]() { named_bar_sync(lane_bar, kIntraThreads); };
     const int4 ent = cx.chunk(c);
     const int t0 = ent.y, len = ent.z;
-    uint8_t* rec = records + ((size_t)slot * H + h) * Rec::bytes;
-
-    const uint32_t raw = smem_u32(smem_raw);
-    uint8_t* sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
     const uint32_t sb = smem_u32(sm);
     float* refs = reinterpret_cast<float*>(sm + M::REFS);
     float* tot = reinterpret_cast<float*>(sm + M::FAC);
@@ -203,41 +194,54 @@ kda_intra_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     float* X = reinterpret_cast<float*>(sm + M::X);
     float* CF = reinterpret_cast<float*>(sm + M::CF);
     float* betas = reinterpret_cast<float*>(sm + M::BETA);
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int warp = tid >> 5, lane = tid & 31;
     const int dc = tid & 15, rg = tid >> 4;  // 8 key channels 8dc.., rows 4rg..4rg+3
     const int P = dc >> 3, cc = dc & 7;      // key panel, chunk within the panel row
     const int swap = (dc >> 2) & 1;
 
-    if (warp == 0) tmem_alloc(&tmem_base, 256);
+    // k counts the chunk-heads this lane has run: the mbarriers are set up once and then
+    // keep their phases (bar_tma and bar_wu complete once per chunk-head, bar_rel twice).
+    // The previous chunk-head's shared-memory accesses are ordered before this one's
+    // tensor-copy writes by the proxy fence.
     if (tid == 0) {
-        s_abort = 0;
-        mbar_init(&bar_tma, 1);
-        mbar_init(&bar_rel, 1);
-        mbar_init(&bar_wu, 1);
-        fence_barrier_init();
+        s_abort_l[lid] = 0;
+        if (k == 0) {
+            mbar_init(&bar_tma, 1);
+            mbar_init(&bar_rel, 1);
+            mbar_init(&bar_wu, 1);
+            fence_barrier_init();
+        }
     }
+    fence_proxy_async_smem();
     tc_fence_before();
-    __syncthreads();
+    lane_sync();
     tc_fence_after();
-    const uint32_t tmem = tmem_base;
-    volatile int* abort_flag = &s_abort;
+    volatile int* abort_flag = &s_abort_l[lid];
 
     // a1: tiles by TMA (rows past the end of the tensor read as zero)
     if (tid == 0) {
         mbar_arrive_expect_tx(&bar_tma, 3 * 16384 + 32768);
         for (int p = 0; p < 2; ++p)
             for (int pp = 0; pp < 2; ++pp)
-                tma_load_2d(sm + M::RB + (p * 2 + pp) * 8192, &tm_q, h * 128 + 64 * pp, t0 + 32 * p,
+                tma_load_2d(sm + M::RB + (p * 2 + pp) * 8192, tmq, h * 128 + 64 * pp, t0 + 32 * p,
                             &bar_tma);
         for (int pp = 0; pp < 2; ++pp) {
-            tma_load_2d(sm + M::KT + pp * 8192, &tm_k, h * 128 + 64 * pp, t0, &bar_tma);
-            tma_load_2d(sm + M::VT + pp * 8192, &tm_v, h * 128 + 64 * pp, t0, &bar_tma);
+            tma_load_2d(sm + M::KT + pp * 8192, tmk, h * 128 + 64 * pp, t0, &bar_tma);
+            tma_load_2d(sm + M::VT + pp * 8192, tmv, h * 128 + 64 * pp, t0, &bar_tma);
         }
-        tma_load_2d(sm + M::RA, &tm_g, h * 128, t0, &bar_tma);
+        tma_load_2d(sm + M::RA, tmg, h * 128, t0, &bar_tma);
+        // the previous record of this lane is published while the tiles load: its bulk
+        // stores complete, then its flag is set with release semantics
+        if (prev_flag) {
+            bulk_wait_all();
+            fence_proxy_async_global();
+            __threadfence();
+            st_release_gpu(prev_flag, 1);
+        }
     }
     if (tid < 64) betas[tid] = tid < len ? beta[(size_t)(t0 + tid) * H + h] : 0.f;
-    mbar_wait_abortable(&bar_tma, 0, status, abort_flag);
-    __syncthreads();
+    mbar_wait_abortable(&bar_tma, k & 1u, status, abort_flag);
+    lane_sync();
     if (*abort_flag) goto teardown;
 
     {
@@ -262,7 +266,7 @@ kda_intra_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
 #pragma unroll
             for (int m = 0; m < 8; ++m) G[r][m] += G[r - 1][m];
         st8f(tot + rg * 128 + dc * 8, G[3]);
-        __syncthreads();
+        lane_sync();
         // exclusive scan of the 16 row-group totals down each key channel (one thread per
         // channel), in place
         if (tid < 128) {
@@ -274,7 +278,7 @@ kda_intra_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 run += t;
             }
         }
-        __syncthreads();
+        lane_sync();
         {
             float pre[8];
             ld8f(tot + rg * 128 + dc * 8, swap, pre);
@@ -285,7 +289,7 @@ kda_intra_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         }
         if ((rg & 3) == 0) st8f(refs + (rg >> 2) * 128 + dc * 8, G[0]);
         if (rg == 15) st8f(refs + 4 * 128 + dc * 8, G[3]);
-        __syncthreads();
+        lane_sync();
 
         // block factors (overwrite the scan totals) and gamma^C = 2^{G_63}: threads 0-127
         // take P0 and gamma of channel d, threads 128-255 the X and C tables of channel d
@@ -308,7 +312,7 @@ kda_intra_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 for (int b = 0; b < 4; ++b) CF[b * 128 + d] = exp2f(gr[4] - gr[b]);
             }
         }
-        __syncthreads();
+        lane_sync();
 
         // a3/a4 operands, row by row (the 4 rows of a thread lie in one 16-row block b)
         float R[4][8];  // key factor rows k_j 2^{G_16b(j) - G_j}, kept for the second round
@@ -318,18 +322,14 @@ kda_intra_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         ld8f(P0 + b * 128 + dc * 8, swap, p0);
         ld8f(CF + b * 128 + dc * 8, swap, cf);
         if (b == 0) ld8f(X + pair_index(1, 0) * 128 + dc * 8, swap, x10);
-        // the shared-memory loads of two rows are issued before their first store
         uint4 qr[2], kr[2], vr[2];
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-            if ((r & 1) == 0) {
-#pragma unroll
-                for (int rr = 0; rr < 2; ++rr) {
-                    const int i = 4 * rg + r + rr;
-                    qr[rr] = lds128(sm, M::RB + ((i >> 5) * 2 + P) * 8192 + sw128_chunk(i & 31, cc));
-                    kr[rr] = lds128(sm, M::KT + P * 8192 + sw128_chunk(i, cc));
-                    vr[rr] = lds128(sm, M::VT + P * 8192 + sw128_chunk(i, cc));
-                }
+            {
+                const int i = 4 * rg + r;
+                qr[r & 1] = lds128(sm, M::RB + ((i >> 5) * 2 + P) * 8192 + sw128_chunk(i & 31, cc));
+                kr[r & 1] = lds128(sm, M::KT + P * 8192 + sw128_chunk(i, cc));
+                vr[r & 1] = lds128(sm, M::VT + P * 8192 + sw128_chunk(i, cc));
             }
             const int i = 4 * rg + r, grp = i >> 5, ii = i & 31;
             const float inb = i < len ? 1.f : 0.f;
@@ -397,18 +397,19 @@ kda_intra_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        __syncthreads();
+        lane_sync();
 
         // relation round 0: query blocks 0 and 1 -> TMEM columns 0-63
-        if (tid == 0) {
+        if (warp == 0) {
             tc_fence_after();
             const uint32_t idesc = idesc_bf16(128, 64);
+#pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 const int pp = ks >> 2, kk = ks & 3;
-                mma_bf16(tmem, desc_sw128(sb + M::RA + pp * 16384 + kk * 32),
-                         desc_sw128(sb + M::RB + pp * 8192 + kk * 32), idesc, ks > 0 ? 1u : 0u);
+                mma_bf16_w(tmem, desc_sw128(sb + M::RA + pp * 16384 + kk * 32),
+                           desc_sw128(sb + M::RB + pp * 8192 + kk * 32), idesc, ks > 0 ? 1u : 0u);
             }
-            mma_commit(&bar_rel);
+            mma_commit_w(&bar_rel);
         }
         mbar_wait_abortable(&bar_rel, 0, status, abort_flag);
         tc_fence_after();
@@ -441,21 +442,22 @@ kda_intra_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     }
     fence_proxy_async_smem();
     tc_fence_before();
-    __syncthreads();
+    lane_sync();
     if (*abort_flag) goto teardown;
-    if (tid == 0) {  // relation round 1: query blocks 2 and 3 -> TMEM columns 64-127
+    if (warp == 0) {  // relation round 1: query blocks 2 and 3 -> TMEM columns 64-127
         tc_fence_after();
         const uint32_t idesc = idesc_bf16(128, 64);
+#pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
             const int pp = ks >> 2, kk = ks & 3;
-            mma_bf16(tmem + 64, desc_sw128(sb + M::RA + pp * 16384 + kk * 32),
-                     desc_sw128(sb + M::RB + (2 + pp) * 8192 + kk * 32), idesc, ks > 0 ? 1u : 0u);
+            mma_bf16_w(tmem + 64, desc_sw128(sb + M::RA + pp * 16384 + kk * 32),
+                       desc_sw128(sb + M::RB + (2 + pp) * 8192 + kk * 32), idesc, ks > 0 ? 1u : 0u);
         }
-        mma_commit(&bar_rel);
+        mma_commit_w(&bar_rel);
     }
     mbar_wait_abortable(&bar_rel, 1, status, abort_flag);
     tc_fence_after();
-    __syncthreads();
+    lane_sync();
     if (*abort_flag) goto teardown;
 
     {
@@ -482,7 +484,7 @@ kda_intra_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             }
         }
         tc_fence_before();
-        __syncthreads();
+        lane_sync();
 
         // a4: (I + L)^{-1} (Tokamax design doc 4.1.4 expands the same block inverse with
         // MXU products).  L = Lb + F with Lb the strictly lower parts of the 16 x 16
@@ -527,7 +529,7 @@ kda_intra_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             else { r = 32 + (t - 160) / 2; ch = 6 + (t - 160) % 2; }
             sts128(sm, M::AIA + sw128_chunk(r, ch), make_uint4(0u, 0u, 0u, 0u));
         }
-        __syncthreads();
+        lane_sync();
 
         // Block products: one warp per 16 x 16 result, acc[nt] the two m16n8 tiles.
         // Pair order of the blocks below the diagonal: (1,0) (2,0) (2,1) (3,0) (3,1) (3,2).
@@ -576,7 +578,7 @@ kda_intra_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             blk_mma(acc, DB + bi * kBlk, kBs, LF + (16 * bi) * kLs + 16 * bj, kLs, 1.f);
             acc_store(acc, JB + pi * kBlk);
         }
-        __syncthreads();
+        lane_sync();
         // Stage 3 (warps 0-2): X20 = J21 J10 - J20, X31 = J32 J21 - J31,
         // X30 = J31 J10 + J32 J20 - J30 - J32 (J21 J10) (warp 2, through a scratch block).
         if (warp < 3) {
@@ -602,7 +604,7 @@ kda_intra_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
                 acc_store(acc, XB + 2 * kBlk);
             }
         }
-        __syncthreads();
+        lane_sync();
         // Stage 5 (warps 0-5, warp = pair): (I + L)^{-1}_ij = X_ij D_j, written as bf16;
         // X_10 = -J10, X_21 = -J21, X_32 = -J32.
         if (warp < 6) {
@@ -621,7 +623,7 @@ kda_intra_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        __syncthreads();
+        lane_sync();
     }
 
     // W = (I+L)^{-1} D_beta K+ (M 128 tokens, 64 used; K 64) with B the token-major k
@@ -631,30 +633,36 @@ kda_intra_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     //    token-major v tile read as MN-major), N 64 tokens (B = (I+L)^{-1} itself, K-major)
     //    -> columns 128-191, so the recurrence reads U^T rows.
     // The same thread then stores Aqk to the record, overlapping the products.
-    if (tid == 0) {
+    if (warp == 0) {
         tc_fence_after();
         if constexpr (Rec::sliced) {
             const uint32_t idesc = idesc_bf16(128, 256, false, true);
+#pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-                mma_bf16(tmem, desc_sw128(sb + M::AIA + kk * 32),
-                         desc_sw128_mn(sb + M::KT + kk * 2048, 8192, 1024), idesc, kk > 0 ? 1u : 0u);
+                mma_bf16_w(tmem, desc_sw128(sb + M::AIA + kk * 32),
+                           desc_sw128_mn(sb + M::KT + kk * 2048, 8192, 1024), idesc, kk > 0 ? 1u : 0u);
         } else {
             const uint32_t id_w = idesc_bf16(128, 128, false, true);
             const uint32_t id_u = idesc_bf16(128, 64, true, false);
+#pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-                mma_bf16(tmem, desc_sw128(sb + M::AIA + kk * 32),
-                         desc_sw128_mn(sb + M::KT + kk * 2048, 8192, 1024), id_w, kk > 0 ? 1u : 0u);
+                mma_bf16_w(tmem, desc_sw128(sb + M::AIA + kk * 32),
+                           desc_sw128_mn(sb + M::KT + kk * 2048, 8192, 1024), id_w, kk > 0 ? 1u : 0u);
+#pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-                mma_bf16(tmem + 128, desc_sw128_mn(sb + M::VT + kk * 2048, 8192, 1024),
-                         desc_sw128(sb + M::AIA + kk * 32), id_u, kk > 0 ? 1u : 0u);
+                mma_bf16_w(tmem + 128, desc_sw128_mn(sb + M::VT + kk * 2048, 8192, 1024),
+                           desc_sw128(sb + M::AIA + kk * 32), id_u, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&bar_wu);
-        bulk_store(rec + Rec::aqk, sm + M::AQS, 8192);
-        bulk_commit();
+        mma_commit_w(&bar_wu);
+        if (lane == 0) {
+            bulk_store(rec + Rec::aqk, sm + M::AQS, 8192);
+            bulk_commit();
+        }
+        __syncwarp();
     }
-    mbar_wait_abortable(&bar_wu, 0, status, abort_flag);
+    mbar_wait_abortable(&bar_wu, k & 1u, status, abort_flag);
     tc_fence_after();
-    __syncthreads();
+    lane_sync();
     if (*abort_flag) goto teardown;
 
     // W rows (warps 0,1; lane = token, 128 keys) into the token-major staging tile of the
@@ -692,7 +700,7 @@ kda_intra_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     }
     fence_proxy_async_smem();
     tc_fence_before();
-    __syncthreads();
+    lane_sync();
     if (tid == 0) {
         bulk_store(rec + Rec::wq, sm + M::WST, 8192);
         bulk_store(rec + Rec::wq + 16384, sm + M::WST + 8192, 8192);
@@ -703,15 +711,58 @@ kda_intra_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
             bulk_store(rec + TcRecord::ut, sm + M::UTS, 16384);
         }
         bulk_commit();
-        // only the shared-memory sources must outlive the copies; the stores themselves
-        // are complete for any later kernel on the stream
+        // only the shared-memory sources must outlive the copies here; a record that is
+        // published is waited for when the next one's tiles load (or after the last)
         bulk_wait_read_all();
     }
+    if (publish) __threadfence();  // this thread's direct stores into the record
 
 teardown:
     tc_fence_before();
+    lane_sync();
+    return *abort_flag == 0;
+}
+
+template <bool kOpts, typename Rec>
+__global__ void __launch_bounds__(kIntraThreads, 2)
+kda_intra_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
+             const float* __restrict__ beta, float scale, GateArgs ga, int H, ChunkIndex cx,
+             long long max_chunks, RangeArgs ra, uint8_t* __restrict__ records,
+             int* __restrict__ status) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ uint32_t tmem_base;
+    const long long blk = blockIdx.x;
+    const int h = (int)(blk % H);
+    long long c, slot;
+    if (ra.span == 0) {
+        // whole problem: chunks from the last to the first, so that the records of early
+        // chunks, which the recurrence reads first, are the most recently written
+        c = max_chunks - 1 - blk / H;
+        if (c >= cx.num_chunks(max_chunks)) return;
+        slot = c;
+    } else {
+        // chunks j0 <= j < j0 + span of every sequence (j = index within the sequence)
+        const long long rest = blk / H;
+        const int jj = (int)(rest % ra.span), n = (int)(rest / ra.span);
+        const int2 sq = cx.seq(n);
+        if (ra.j0 + jj >= sq.y) return;
+        c = sq.x + ra.j0 + jj;
+        slot = (long long)n * ra.span + jj;
+    }
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    if (threadIdx.x < 32) tmem_alloc(&tmem_base, 256);
+    tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 256);
+    tc_fence_after();
+    const uint32_t tmem = __shfl_sync(0xffffffffu, tmem_base, 0);
+    intra_unit<kOpts, Rec, 0>(&tm_q, &tm_k, &tm_v, &tm_g, beta, scale, ga, H, cx, c, h,
+                              records + ((size_t)slot * H + h) * Rec::bytes, nullptr, false, sm, tmem,
+                              0, threadIdx.x, 0u, status);
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x < 32) tmem_dealloc(tmem, 256);
 }
 
 // ---------------------------------------------------------------------------
@@ -751,17 +802,21 @@ __device__ __forceinline__ void tmem_st16_wait(uint32_t taddr, const uint32_t (&
         : "memory");
 }
 
-__global__ void __launch_bounds__(kHoThreads, 1)
-kda_h_o_tc(const uint8_t* __restrict__ records, ChunkIndex cx, long long max_chunks, RangeArgs ra,
-           const float* __restrict__ s0, __nv_bfloat16* __restrict__ o, float* __restrict__ sN,
-           int H, int* __restrict__ status) {
+// The chain (sequence n, head h) of the per-chain recurrence, run by the whole CTA (at
+// least kHoThreads threads; warps past the roles idle).  With `flags`, the records are
+// produced by other CTAs of the same launch: a loader warp polls each record's flag
+// before copying it, and a stage is refilled once the products that read it are done.
+template <bool kPublished>
+__device__ __forceinline__ void ho_chain(int n, int h, const int* __restrict__ flags,
+                                         const uint8_t* __restrict__ records, const ChunkIndex& cx,
+                                         long long max_chunks, const RangeArgs& ra,
+                                         const float* __restrict__ s0, __nv_bfloat16* __restrict__ o,
+                                         float* __restrict__ sN, int H, int* __restrict__ status) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t full[kStages], bar_m1, bar_m3, bar_m2[2], bar_out[2];
+    __shared__ uint64_t full[kStages], empty[kStages], bar_m1, bar_m3, bar_m2[2], bar_out[2];
     __shared__ uint32_t tmem_base;
     __shared__ int s_abort;
 
-    const int h = blockIdx.x % H;
-    const int n = blockIdx.x / H;
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
     const uint32_t sb = smem_u32(sm);
@@ -791,7 +846,10 @@ kda_h_o_tc(const uint8_t* __restrict__ records, ChunkIndex cx, long long max_chu
     if (warp == 0) tmem_alloc(&tmem_base, 512);
     if (tid == 0) {
         s_abort = 0;
-        for (int i = 0; i < kStages; ++i) mbar_init(&full[i], 1);
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
         mbar_init(&bar_m1, 1);
         mbar_init(&bar_m3, 1);
         mbar_init(&bar_m2[0], 1);
@@ -806,7 +864,30 @@ kda_h_o_tc(const uint8_t* __restrict__ records, ChunkIndex cx, long long max_chu
     const uint32_t tmem = tmem_base;
     volatile int* abort_flag = &s_abort;
 
-    if (warp >= kOutWarp0) {
+    if (warp >= kOutWarp0 + 4) {
+        // ---- loader warp (published records only): copy record ci into stage ci % 3
+        // once its flag is set and the products of chunk ci - 3 are done ----
+        if (kPublished && warp == kOutWarp0 + 4 && lane == 0) {
+            for (int ci = 0; ci < nch; ++ci) {
+                const int sg = ci % kStages;
+                if (ci >= kStages &&
+                    !mbar_wait_abortable(&empty[sg], ((ci / kStages) - 1) & 1, status, abort_flag))
+                    break;
+                const int* f = flags + (size_t)(first + ci) * H + h;
+                uint32_t it = 0;
+                while (ld_acquire_gpu(f) == 0 && *abort_flag == 0 && ++it < kWaitLimit) __nanosleep(128);
+                if (it >= kWaitLimit) {
+                    atomicCAS(status, 0, (int)KDA_ERR_DEVICE_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                if (*abort_flag) break;
+                fence_proxy_async_global();
+                mbar_arrive_expect_tx(&full[sg], TcRecord::used);
+                bulk_load(sm + sg * kStage, rec_of(ci), TcRecord::used, &full[sg]);
+            }
+        }
+        __syncwarp();
+    } else if (warp >= kOutWarp0) {
         // ---- output warps: O^T of chunk ci from D1 columns 64-127 (lane = value v, all 64
         // query rows), read while the chain goes on, then the D1 buffer is handed back ----
         // a warp reaches only the TMEM lanes of its own sub-partition (warp % 4)
@@ -840,7 +921,7 @@ kda_h_o_tc(const uint8_t* __restrict__ records, ChunkIndex cx, long long max_chu
             mbar_arrive_expect_tx(&full[sg], TcRecord::used);
             bulk_load(sm + sg * kStage, rec_of(ci), TcRecord::used, &full[sg]);
         };
-        if (lane == 0)
+        if (lane == 0 && !kPublished)
             for (int ci = 0; ci < kStages && ci < nch; ++ci) load(ci);
         __syncwarp();
         const uint32_t id_1 = idesc_bf16(128, 128, false, false);  // D1 = S^T [W ; Qg]^T
@@ -854,23 +935,25 @@ kda_h_o_tc(const uint8_t* __restrict__ records, ChunkIndex cx, long long max_chu
             if (!__all_sync(0xffffffffu, ok)) break;
             named_bar_sync(kBarState, kChainThreads);  // S_ci^T in tensor memory
             if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+            // chunk ci - 1's stage is free once its products are done (the commit tracks
+            // them) and its epilogue, which reads gamma there, has passed the sync above
+            if (kPublished && ci >= 1) mma_commit_w(&empty[(ci - 1) % kStages]);
             if (ci >= 2) {  // D1 buffer of chunk ci-2 read by the output warps
                 ok = mbar_wait_abortable(&bar_out[ci & 1], ((ci - 2) >> 1) & 1, status, abort_flag);
                 if (!__all_sync(0xffffffffu, ok)) break;
             }
-            if (lane == 0) {
-                tc_fence_after();
-                // MMA1: D1 = S^T [W ; Qg]^T   (K = 128 keys: A 8 columns per step, B two
-                // K-major panels)
-                for (int ks = 0; ks < 8; ++ks)
-                    mma_bf16_ta(D1, tmem + kColS + 8 * ks,
-                                desc_sw128(stb + TcRecord::wq + (ks >> 2) * 16384 + (ks & 3) * 32),
-                                id_1, ks > 0 ? 1u : 0u);
-                mma_commit(&bar_m1);
-            }
+            tc_fence_after();
+            // MMA1: D1 = S^T [W ; Qg]^T   (K = 128 keys: A 8 columns per step, B two
+            // K-major panels)
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                mma_bf16_ta_w(D1, tmem + kColS + 8 * ks,
+                              desc_sw128(stb + TcRecord::wq + (ks >> 2) * 16384 + (ks & 3) * 32),
+                              id_1, ks > 0 ? 1u : 0u);
+            mma_commit_w(&bar_m1);
             __syncwarp();
             // refill the stage chunk ci-1 used: its MMA2 precedes this MMA1 on the pipe
-            if (ci >= 1 && ci - 1 + kStages < nch) {
+            if (!kPublished && ci >= 1 && ci - 1 + kStages < nch) {
                 ok = mbar_wait_abortable(&bar_m2[(ci - 1) & 1], ((ci - 1) >> 1) & 1, status, abort_flag);
                 if (!__all_sync(0xffffffffu, ok)) break;
                 if (lane == 0) load(ci - 1 + kStages);
@@ -878,20 +961,22 @@ kda_h_o_tc(const uint8_t* __restrict__ records, ChunkIndex cx, long long max_chu
             }
             named_bar_sync(kBarVnew, kChainThreads);  // V_new^T in tensor memory
             if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
-            if (lane == 0) {
-                tc_fence_after();
+            tc_fence_after();
+            {
                 // MMA3 first (it feeds the state): D3 = V_new^T K_bar (K = 64 tokens; K_bar
                 // token-major: MN-major B, 2 atoms 8 KB apart)
                 const uint64_t dKB = desc_sw128_mn(stb + TcRecord::kb0, 8192, 1024);
+#pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16_ta(tmem + kColD3, tmem + kColVn + 8 * kk,
-                                dKB + (uint64_t)((kk * 2048) >> 4), id_3, kk > 0 ? 1u : 0u);
-                mma_commit(&bar_m3);
+                    mma_bf16_ta_w(tmem + kColD3, tmem + kColVn + 8 * kk,
+                                  dKB + (uint64_t)((kk * 2048) >> 4), id_3, kk > 0 ? 1u : 0u);
+                mma_commit_w(&bar_m3);
                 // MMA2: D1 columns 64-127 += V_new^T Aqk^T  (O^T = (Qg S)^T + (Aqk V_new)^T)
+#pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16_ta(D1 + 64, tmem + kColVn + 8 * kk,
-                                desc_sw128(stb + TcRecord::aqk + kk * 32), id_2, 1u);
-                mma_commit(&bar_m2[ci & 1]);
+                    mma_bf16_ta_w(D1 + 64, tmem + kColVn + 8 * kk,
+                                  desc_sw128(stb + TcRecord::aqk + kk * 32), id_2, 1u);
+                mma_commit_w(&bar_m2[ci & 1]);
             }
             __syncwarp();
         }
@@ -984,6 +1069,116 @@ kda_h_o_tc(const uint8_t* __restrict__ records, ChunkIndex cx, long long max_chu
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+__global__ void __launch_bounds__(kHoThreads, 1)
+kda_h_o_tc(const uint8_t* __restrict__ records, ChunkIndex cx, long long max_chunks, RangeArgs ra,
+           const float* __restrict__ s0, __nv_bfloat16* __restrict__ o, float* __restrict__ sN,
+           int H, int* __restrict__ status) {
+    ho_chain<false>(blockIdx.x / H, blockIdx.x % H, nullptr, records, cx, max_chunks, ra, s0, o, sN, H, status);
+}
+
+// Fused schedule for few chains of fixed-length sequences: one persistent CTA per SM.
+// CTAs 0 .. nc - 1 each run the per-chain recurrence of chain b = n H + h; every other
+// CTA runs two intra lanes, which work through the chunk-heads in chunk-major order
+// (chunk 0 of every chain first, as the recurrences consume them) and publish each record
+// through its flag.  The recurrence CTAs poll those flags, so the launch is cooperative:
+// all CTAs are resident, and a producer never waits for a consumer.
+constexpr int kFusedThreads = 2 * kIntraThreads;
+static_assert(kFusedThreads >= kHoThreads + 32, "fused CTA must hold the recurrence roles and its loader");
+constexpr uint32_t kIntraLane = (uint32_t)((IntraMap::END + 1023) / 1024 * 1024);
+constexpr size_t kFusedSmem =
+    (2ull * kIntraLane > (size_t)kStages * kStage ? 2ull * kIntraLane : (size_t)kStages * kStage) + 1024;
+static_assert(kFusedSmem <= 232448, "fused kernel exceeds the shared-memory limit");
+
+// The recurrence role of the fused kernel, compiled as its own function so that its
+// registers are allocated apart from the intra lanes'.
+__device__ __noinline__ void ho_chain_published(int n, int h, const int* __restrict__ flags,
+                                                const uint8_t* __restrict__ records,
+                                                const ChunkIndex& cx, long long max_chunks,
+                                                const float* __restrict__ s0,
+                                                __nv_bfloat16* __restrict__ o, float* __restrict__ sN,
+                                                int H, int* __restrict__ status) {
+    ho_chain<true>(n, h, flags, records, cx, max_chunks, RangeArgs{}, s0, o, sN, H, status);
+}
+
+// Arguments of the fused kernel (one grid-constant block, read in place by both roles).
+struct FusedArgs {
+    CUtensorMap tq, tk, tv, tg;
+    const float* beta;
+    float scale;
+    GateArgs ga;
+    int H;
+    ChunkIndex cx;
+    long long max_chunks;
+    uint8_t* records;
+    int* flags;
+    const float* s0;
+    __nv_bfloat16* o;
+    float* sN;
+    int nc;
+    int* status;
+};
+
+// One intra lane of the fused kernel: units u0, u0 + lanes, ... (chunk j = u / nc of chain
+// u % nc), each record published when the next one's tiles load (the last at the end).
+// Both lanes of a CTA run the same code (one copy: the kernel is large, and instruction
+// fetch stalls when the SM alternates between two copies).
+template <bool kOpts>
+__device__ __forceinline__ void intra_lane(const FusedArgs& A, uint8_t* sm, uint32_t tmem, int lid, int tid) {
+    const int nc = A.nc, H = A.H;
+    const long long u0 = 2ll * ((long long)blockIdx.x - nc) + lid;
+    const long long lanes = 2ll * ((long long)gridDim.x - nc);
+    const long long units = (long long)nc * A.cx.nct;
+    auto chunk_of = [&](long long u) { return (long long)((int)(u % nc) / H) * A.cx.nct + (int)(u / nc); };
+    uint32_t k = 0;
+    bool ok = true;
+#pragma unroll 1
+    for (long long u = u0; u < units; u += lanes, ++k) {
+        // the thread index goes through an empty asm each unit, so that the compiler
+        // derives the per-thread offsets inside the unit instead of holding them across
+        // the loop (registers are the intra lane's limit)
+        int tid_u = tid;
+        asm volatile("" : "+r"(tid_u));
+        int* prev = k > 0 ? A.flags + (size_t)chunk_of(u - lanes) * H + (int)((u - lanes) % nc) % H : nullptr;
+        const long long c = chunk_of(u);
+        const int h = (int)(u % nc) % H;
+        ok = intra_unit<kOpts, TcRecord, -1>(&A.tq, &A.tk, &A.tv, &A.tg, A.beta, A.scale, A.ga, H, A.cx,
+                                             c, h, A.records + ((size_t)c * H + h) * TcRecord::bytes,
+                                             prev, true, sm, tmem, lid, tid_u, k, A.status);
+        if (!ok) break;
+    }
+    if (ok && k > 0 && tid == 0) {  // the lane's last record
+        const long long ul = u0 + (long long)(k - 1) * lanes;
+        bulk_wait_all();
+        fence_proxy_async_global();
+        __threadfence();
+        st_release_gpu(A.flags + (size_t)chunk_of(ul) * H + (int)(ul % nc) % H, 1);
+    }
+}
+
+template <bool kOpts>
+__global__ void __launch_bounds__(kFusedThreads, 1) kda_fused_tc(const __grid_constant__ FusedArgs A) {
+    const int nc = A.nc, H = A.H;
+    if ((int)blockIdx.x < nc) {
+        ho_chain_published((int)blockIdx.x / H, (int)blockIdx.x % H, A.flags, A.records, A.cx,
+                           A.max_chunks, A.s0, A.o, A.sN, H, A.status);
+        return;
+    }
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ uint32_t tmem_base;
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    const int lid = (int)threadIdx.x / kIntraThreads, tid = (int)threadIdx.x % kIntraThreads;
+    if (threadIdx.x < 32) tmem_alloc(&tmem_base, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = __shfl_sync(0xffffffffu, tmem_base, 0);
+    intra_lane<kOpts>(A, sm + lid * kIntraLane, tbase + 256u * (uint32_t)lid, lid, tid);
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x < 32) tmem_dealloc(tbase, 512);
 }
 
 // Value-sliced recurrence: one CTA (8 epilogue warps + 1 issuer warp) per (sequence,
@@ -1104,14 +1299,15 @@ kda_h_o_sliced_tc(const uint8_t* __restrict__ records, ChunkIndex cx, long long 
             if (!__all_sync(0xffffffffu, ok)) break;
             named_bar_sync(kBarState, kHoThreads);  // S_ci written, D1/D3 of earlier chunks read
             if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
-            if (lane == 0) {
-                tc_fence_after();
+            tc_fence_after();
+            {
                 // MMA1: D1 = [W ; Qg] S   (K = 128 keys over two panels)
                 const uint64_t dWQ = desc_sw128(stb + WQ);
+#pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
-                    mma_bf16(D1, dWQ + (uint64_t)(((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
-                             dS + (uint64_t)((ks * 2048) >> 4), idesc_a, ks > 0 ? 1u : 0u);
-                mma_commit(&bar_m1);
+                    mma_bf16_w(D1, dWQ + (uint64_t)(((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
+                               dS + (uint64_t)((ks * 2048) >> 4), idesc_a, ks > 0 ? 1u : 0u);
+                mma_commit_w(&bar_m1);
             }
             __syncwarp();
             // refill the stage chunk ci-1 used: its MMA2 precedes this MMA1 on the pipe
@@ -1123,21 +1319,23 @@ kda_h_o_sliced_tc(const uint8_t* __restrict__ records, ChunkIndex cx, long long 
             }
             named_bar_sync(kBarVnew, kVnewCount);  // V_new tile written
             if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
-            if (lane == 0) {
-                tc_fence_after();
+            tc_fence_after();
+            {
                 // MMA3 first (it feeds the state): D3 = K_bar^T V_new (K_bar token-major:
                 // MN-major A, 2 atoms 8 KB apart)
                 const uint64_t dKB = desc_sw128_mn(stb + KB, 8192, 1024);
+#pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(D3, dKB + (uint64_t)((kk * 2048) >> 4),
-                             dVN + (uint64_t)((kk * 2048) >> 4), idesc_t, kk > 0 ? 1u : 0u);
-                mma_commit(&bar_m3);
+                    mma_bf16_w(D3, dKB + (uint64_t)((kk * 2048) >> 4),
+                               dVN + (uint64_t)((kk * 2048) >> 4), idesc_t, kk > 0 ? 1u : 0u);
+                mma_commit_w(&bar_m3);
                 // MMA2: D1 += [Qg panel-1 rows ; Aqk] V_new  (only rows 64-127 are used)
                 const uint64_t dQA = desc_sw128(stb + AQK - 8192);
+#pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(D1, dQA + (uint64_t)((kk * 32) >> 4),
-                             dVN + (uint64_t)((kk * 2048) >> 4), idesc_a, 1u);
-                mma_commit(&bar_m2[ci & 1]);
+                    mma_bf16_w(D1, dQA + (uint64_t)((kk * 32) >> 4),
+                               dVN + (uint64_t)((kk * 2048) >> 4), idesc_a, 1u);
+                mma_commit_w(&bar_m2[ci & 1]);
             }
             __syncwarp();
         }
@@ -1346,6 +1544,28 @@ cudaError_t launch_tc(const void* q, const void* k, const void* v, const float* 
         cudaFuncSetAttribute(intra, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kIntraSmem);
     cudaFuncSetAttribute(ho, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ho_smem);
     __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(o);
+
+    // Fused schedule: one cooperative launch, one CTA per SM (the recurrence CTAs poll
+    // flags the other CTAs set, so all CTAs must be resident); the flags start cleared.
+    if (L.fused && !ev) {
+        int* flags = reinterpret_cast<int*>(ws + L.flags_off);
+        if (cudaError_t e = cudaMemsetAsync(flags, 0, (size_t)L.max_chunks * H * sizeof(int), s)) return e;
+        auto* fk = opts ? kda_fused_tc<true> : kda_fused_tc<false>;
+        if (cudaError_t e = cudaFuncSetAttribute(fk, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)kFusedSmem))
+            return e;
+        int per_sm = 0;
+        if (cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fk, kFusedThreads,
+                                                                          kFusedSmem))
+            return e;
+        int nc = L.N * H;
+        if (per_sm < 1 || nc >= sms) return cudaErrorInvalidConfiguration;
+        FusedArgs fa{tq, tk, tv, tg, beta, scale, ga, H, cx, L.max_chunks, records, flags,
+                     s0, ob, sN, nc, status};
+        void* args[] = {&fa};
+        return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(fk), dim3((unsigned)sms),
+                                           dim3(kFusedThreads), args, kFusedSmem, s);
+    }
 
     // Whole-problem schedule: one launch of each kernel (and the only one with per-kernel
     // timing events).

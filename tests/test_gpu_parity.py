@@ -140,14 +140,16 @@ def test_deterministic(kda):
 
 @pytest.mark.parametrize("shape", [(1, 64 * 512, 2, 0.1), (2, 64 * 600 + 37, 1, None)],
                          ids=["512chunks_init", "601chunks_tail"])
-def test_pipelined_schedule(kda, orc, shape):
+def test_pipelined_schedule(kda, orc, shape, monkeypatch):
     """The pipelined schedule (chunk ranges on two streams, state handed over in fp32)
     gives bit-identical results to the whole-problem schedule, and matches the oracle."""
     B, T, H, init = shape
     inp = make_inputs(custom(B=B, T=T, H=H, K=128, V=128, dtype=torch.bfloat16,
                              init_std=init, seed=T + H), device="cuda")
+    monkeypatch.setenv("KDA_SCHEDULE", "pipelined")
     assert kda.launch_count(B, T, H, 128, 128) > 3   # really pipelined
     o_p, f_p = run_gpu(kda, inp)
+    monkeypatch.delenv("KDA_SCHEDULE")
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
     for e in evs:
         e.record()
@@ -168,6 +170,53 @@ def test_per_chain_recurrence_form(kda, orc, shape):
     inp = make_inputs(custom(B=B, T=T, H=H, K=128, V=128, dtype=torch.bfloat16, init_std=init,
                              seed=B + T + H), device="cuda")
     check(kda, orc, inp)
+
+
+@pytest.mark.parametrize("shape", [(2, 4096, 4, None), (3, 64 * 37 + 29, 2, 0.1), (1, 64, 3, 0.1),
+                                   (1, 1, 2, None), (2, 63, 1, 0.1)],
+                         ids=["dense_like", "tail_init", "one_chunk", "one_token", "short"])
+def test_fused_schedule(kda, orc, shape, monkeypatch):
+    """Few chains of fixed-length sequences run fused: one cooperative launch in which
+    some CTAs run the per-chain recurrences while the others produce the records.  It
+    matches the oracle, and the two-kernel schedule (value-sliced recurrence, other
+    operand rounding) to the bf16 tolerance."""
+    B, T, H, init = shape
+    inp = make_inputs(custom(B=B, T=T, H=H, K=128, V=128, dtype=torch.bfloat16,
+                             init_std=init, seed=T * 7 + H), device="cuda")
+    assert kda.launch_count(B, T, H, 128, 128) == 1   # fused
+    o_f, f_f = run_gpu(kda, inp)
+    o_ref, f_ref = run_oracle(orc, inp)
+    eo, ef = errors(o_f, f_f, o_ref, f_ref)
+    assert eo <= 2e-2 and ef <= 2e-2, (eo, ef)
+    monkeypatch.setenv("KDA_SCHEDULE", "two")
+    assert kda.launch_count(B, T, H, 128, 128) == 2
+    o_t, f_t = run_gpu(kda, inp)
+    monkeypatch.delenv("KDA_SCHEDULE")
+    eo, ef = errors(o_t, f_t, o_ref, f_ref)
+    assert eo <= 2e-2 and ef <= 2e-2, (eo, ef)
+    assert (o_f.float() - o_t.float()).abs().max().item() <= 2e-2
+    assert (f_f - f_t).abs().max().item() <= 2e-2
+    o_2, f_2 = run_gpu(kda, inp)                     # repeatable (flags reset per call)
+    assert torch.equal(o_2, o_f) and torch.equal(f_2, f_f)
+
+
+@pytest.mark.parametrize("mode", ["two", "fused"])
+def test_forced_schedules_dense(kda, orc, mode, monkeypatch):
+    """The dense workload's shape under each schedule, checked on a sample of chains."""
+    w = WORKLOADS["dense_bf16"]
+    inp = make_inputs(w, device="cuda")
+    monkeypatch.setenv("KDA_SCHEDULE", mode)
+    o, fin = run_gpu(kda, inp)
+    monkeypatch.delenv("KDA_SCHEDULE")
+    for b, h in ((0, 0), (1, 15), (1, 7)):
+        one = {k_: (v_[b:b + 1, :, h:h + 1].contiguous() if k_ in ("q", "k", "v", "g", "beta") else v_)
+               for k_, v_ in inp.items()}
+        one["initial_state"] = None
+        one["cu_seqlens"] = None
+        o_ref, f_ref = run_oracle(orc, {**one, "T": one["q"].shape[1]})
+        eo = float(np.max(np.abs(o[b:b + 1, :, h:h + 1].float().cpu().numpy() - o_ref)))
+        ef = float(np.max(np.abs(fin[b:b + 1, h:h + 1].cpu().numpy() - f_ref)))
+        assert eo <= 2e-2 and ef <= 2e-2, (b, h, eo, ef)
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
