@@ -715,7 +715,10 @@ __device__ __forceinline__ bool intra_unit(const CUtensorMap* tmq, const CUtenso
         // published is waited for when the next one's tiles load (or after the last)
         bulk_wait_read_all();
     }
-    if (publish) __threadfence();  // this thread's direct stores into the record
+    // A published record's direct stores (query and key rows, gamma) by every thread are
+    // ordered before its flag by the lane barriers that follow and the publishing
+    // thread's gpu-scope fence before the release store (the fence is cumulative).
+    (void)publish;
 
 teardown:
     tc_fence_before();
