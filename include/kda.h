@@ -123,15 +123,23 @@ size_t kda_fwd_workspace_bytes(int B, int T, int H, int K, int V, int num_seqs,
  * same inputs give bit-identical outputs, and o at token t does not depend on any
  * input of a later token of the same sequence.
  *
- * Schedule.  The bf16 K = V = 128 path on fixed-length input with at most 128
- * (sequence, head) chains runs pipelined: the chunks of every sequence are cut into
- * ranges, and the intra-chunk kernel of the next range runs on `stream` while the
- * recurrence of the current one runs on a second stream of the library (created once
- * per device with the events it needs; no device memory is allocated).  The second
- * stream forks from and joins back into `stream` through events, so the call stays
- * ordered on `stream` and can be captured into a CUDA graph.  Every other case launches
- * each kernel once over the whole problem.  kda_fwd_launch_count gives the number of
- * kernel launches. */
+ * Schedule (bf16, K = V = 128, fixed-length input; everything else launches each kernel
+ * once over the whole problem):
+ *   fused      at most a third of the SMs' count of (sequence, head) chains: one
+ *              cooperative launch, one CTA per SM; some CTAs run the recurrences and poll
+ *              per-record flags in the workspace (bounded waits) that the other CTAs set
+ *              as they produce the records.  A cudaMemsetAsync of the flags precedes it.
+ *              The workspace size then depends on the current device's SM count.
+ *   pipelined  otherwise, at most 128 chains and at least 512 chunks per sequence: the
+ *              chunks of every sequence are cut into ranges, and the intra-chunk kernel
+ *              of the next range runs on `stream` while the recurrence of the current one
+ *              runs on a second stream of the library (created once per device with the
+ *              events it needs; no device memory is allocated).  The second stream forks
+ *              from and joins back into `stream` through events, so the call stays ordered
+ *              on `stream` and can be captured into a CUDA graph.
+ * The environment variable KDA_SCHEDULE ("two", "pipelined", "fused") forces a schedule
+ * where the sizes allow it (read at workspace sizing and at each call, which must agree).
+ * kda_fwd_launch_count gives the number of kernel launches. */
 kda_status kda_fwd(const void* q, const void* k, const void* v, const float* g,
                    const float* beta, float scale, int chunk_size,
                    const float* initial_state, const int32_t* cu_seqlens, int num_seqs,
@@ -171,8 +179,9 @@ kda_status kda_decode(const void* q, const void* k, const void* v, const float* 
  * still gets its event recorded (fixed-length bf16 input with K = V = 128 has no
  * chunk-index kernel: its chunk positions are arithmetic).  With events the kernels
  * always run back to back on
- * `stream`, one launch each over the whole problem (never the pipelined schedule), so
- * that each stage is one kernel's time; results are identical. */
+ * `stream`, one launch each over the whole problem (never the pipelined or fused
+ * schedule), so that each stage is one kernel's time; results agree to the bf16
+ * tolerance (bit-identical to the pipelined schedule). */
 kda_status kda_fwd_profiled(const void* q, const void* k, const void* v, const float* g,
                             const float* beta, float scale, int chunk_size,
                             const float* initial_state, const int32_t* cu_seqlens,
@@ -245,10 +254,10 @@ kda_status kda_get_device_status(const void* workspace, void* stream);
 kda_status kda_selftest_umma(const void* A, const void* B, float* D, int N, int K, int mode,
                              int* status, void* stream);
 
-/* Number of kernel launches kda_fwd makes for these sizes: the chunk-index kernel
- * (packed input, and the fp32 / other-shape path), the intra-chunk kernel and the
- * recurrence kernel (pipelined calls launch the last two once per chunk range); -1 for
- * sizes kda_fwd rejects. */
+/* Number of kernel launches kda_fwd makes for these sizes on the current device: the
+ * chunk-index kernel (packed input, and the fp32 / other-shape path), the intra-chunk
+ * kernel and the recurrence kernel (pipelined calls launch the last two once per chunk
+ * range; fused calls make one launch); -1 for sizes kda_fwd rejects. */
 int kda_fwd_launch_count(int B, int T, int H, int K, int V, int num_seqs, int chunk_size,
                          kda_dtype dtype);
 
