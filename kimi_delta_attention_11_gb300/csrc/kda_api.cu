@@ -12,7 +12,7 @@
 namespace kda {
 
 // Schedule request from the KDA_SCHEDULE environment variable ("two", "pipelined",
-// "fused"; anything else or unset: automatic).  A forced schedule that does not apply to
+// "fused", "scan"; anything else or unset: automatic).  A forced schedule that does not apply to
 // the sizes falls back to the automatic choice's next option (see make_layout).
 Schedule schedule_request() {
     const char* e = std::getenv("KDA_SCHEDULE");
@@ -20,6 +20,7 @@ Schedule schedule_request() {
     if (!std::strcmp(e, "two")) return Schedule::kTwo;
     if (!std::strcmp(e, "pipelined")) return Schedule::kPipelined;
     if (!std::strcmp(e, "fused")) return Schedule::kFused;
+    if (!std::strcmp(e, "scan")) return Schedule::kScan;
     return Schedule::kAuto;
 }
 
@@ -69,7 +70,27 @@ Layout make_layout(int B, int T, int H, int K, int V, int num_seqs, bool packed,
     // run up to 2 ranges ahead.
     const bool can_pipe = L.fixed && chains <= 128 && nct >= 2;
     const bool auto_pipe = can_pipe && nct >= kPipeMinChunks;
-    if (want == Schedule::kFused ? can_fuse : (want == Schedule::kAuto && auto_fuse)) {
+    // Scan: with very few chains the ordered chunk steps of each chain set the call's time
+    // however fast the records are made, so each sequence is cut into segments whose
+    // affine summaries (Phi, Psi) are formed in parallel, merged per chain, and then
+    // replayed from the merged start states (three chunk-step passes instead of one, all
+    // parallel over segments).  Automatic up to an eighth of the SMs' count of chains and
+    // from 128 chunks per sequence.
+    const bool can_scan = L.fixed && L.max_chunks > 0 && sms > 0 && nct >= 4 && chains <= sms;
+    const bool auto_scan = can_scan && 8 * chains <= sms && nct >= 128;
+    if (want == Schedule::kScan ? can_scan : (want == Schedule::kAuto && auto_scan)) {
+        long long P = sms / (2 * chains);
+        P = P < 2 ? 2 : P;
+        if (P > nct / 2) P = nct / 2;
+        const long long Ls = (nct + P - 1) / P;
+        L.scan = true;
+        L.scan_L = (int)Ls;
+        L.scan_P = (int)((nct + Ls - 1) / Ls);
+        const size_t plane = (size_t)chains * K * V * sizeof(float);
+        L.summ_off = align_up(L.total, 1024);
+        L.starts_off = align_up(L.summ_off + 2 * (size_t)L.scan_P * plane, 1024);
+        L.total = L.starts_off + (size_t)L.scan_P * plane;
+    } else if (want == Schedule::kFused ? can_fuse : (want == Schedule::kAuto && auto_fuse)) {
         L.fused = true;
         L.flags_off = align_up(L.total, 256);
         L.total = L.flags_off + (size_t)L.max_chunks * H * sizeof(int);
@@ -142,6 +163,7 @@ int kda_fwd_launch_count(int B, int T, int H, int K, int V, int num_seqs, int ch
     const Layout L = make_layout(B, T, H, K, V, num_seqs, packed, dtype);
     const int index = L.fixed ? 0 : 1;
     if (L.fused) return 1;
+    if (L.scan) return 4;
     if (L.span > 0) return index + 2 * L.ranges;
     return index + (L.max_chunks > 0 ? 1 : 0) + (L.N > 0 ? 1 : 0);
 }

@@ -14,7 +14,7 @@ constexpr int kChunk = 64;  // chunk size C: the production path fixes C = 64
 constexpr int kPipeMinChunks = 512;  // chunks per sequence from which calls are pipelined
 
 // Launch schedule of a call (see make_layout).
-enum class Schedule { kAuto, kTwo, kPipelined, kFused };
+enum class Schedule { kAuto, kTwo, kPipelined, kFused, kScan };
 
 // Byte layout of the caller's workspace.
 //   [0, 4)       int32 device status word (0 = ok, else a kda_status)
@@ -47,6 +47,13 @@ struct Layout {
     // records, published through one flag word per (chunk, head) at flags_off.
     bool fused = false;
     size_t flags_off = 0;
+    // Chunk-parallel scan schedule (tensor-core path, fixed-length input with very few,
+    // long chains): segments of scan_L chunks, scan_P per sequence; segment summaries
+    // [2][P][chains][K][V] at summ_off, merged segment start states [P][chains][K][V] at
+    // starts_off.
+    bool scan = false;
+    int scan_P = 0, scan_L = 0;
+    size_t summ_off = 0, starts_off = 0;
 };
 
 // Where the kernels find a chunk's sequence, first token, length and index within its

@@ -805,6 +805,19 @@ __device__ __forceinline__ void tmem_st16_wait(uint32_t taddr, const uint32_t (&
         : "memory");
 }
 
+// Chunk-parallel state scan (Tokamax design doc, context-parallel section: the chunk
+// transition S' = Phi_c S + Psi_c with Phi_c = Diag(gamma_c) - K_bar_c^T W_c and
+// Psi_c = K_bar_c^T U_c is affine, so segments compose).  Mode 1 runs segment `seg` of a
+// chain from S = 0 with the chunk's U (var 0: the segment's Psi) or from S = I with U = 0
+// (var 1: its Phi, column by column) and writes the end state to summ; mode 2 runs the
+// segment from its merged start state with the output on.  The recurrence of each column
+// of S is independent of the others, which is what lets the identity start give Phi.
+struct ScanArgs {
+    int mode = 0, P = 0, L = 0, nc = 0;
+    const float* starts = nullptr;  // [P][nc][K][V] segment start states (mode 2)
+    float* summ = nullptr;          // [2][P][nc][K][V] segment end states (mode 1)
+};
+
 // The chain (sequence n, head h) of the per-chain recurrence, run by the whole CTA (at
 // least kHoThreads threads; warps past the roles idle).  With `flags`, the records are
 // produced by other CTAs of the same launch: a loader warp polls each record's flag
@@ -814,7 +827,8 @@ __device__ __forceinline__ void ho_chain(int n, int h, const int* __restrict__ f
                                          const uint8_t* __restrict__ records, const ChunkIndex& cx,
                                          long long max_chunks, const RangeArgs& ra,
                                          const float* __restrict__ s0, __nv_bfloat16* __restrict__ o,
-                                         float* __restrict__ sN, int H, int* __restrict__ status) {
+                                         float* __restrict__ sN, int H, int* __restrict__ status,
+                                         const ScanArgs& sc = ScanArgs{}, int seg = 0, int var = 0) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t full[kStages], empty[kStages], bar_m1, bar_m3, bar_m2[2], bar_out[2];
     __shared__ uint32_t tmem_base;
@@ -834,14 +848,26 @@ __device__ __forceinline__ void ho_chain(int n, int h, const int* __restrict__ f
     // pipelined call); the state comes from initial_state (or zeros) at j = 0, else from
     // the carry buffer, and goes to final_state after the sequence's last chunk, else to
     // the carry buffer
-    const int lo = ra.span ? ra.j0 : 0;
-    const int hi = ra.span ? min(ra.j0 + ra.span, seq_chunks) : seq_chunks;
+    // (scan mode: segment seg of the chain, see ScanArgs)
+    const int lo = sc.mode ? seg * sc.L : (ra.span ? ra.j0 : 0);
+    const int hi = sc.mode ? min(lo + sc.L, seq_chunks) : (ra.span ? min(ra.j0 + ra.span, seq_chunks) : seq_chunks);
     if (lo >= hi && !(lo == 0 && seq_chunks == 0)) return;  // nothing of this sequence here
     const int nch = hi > lo ? hi - lo : 0;
     const long long first = (long long)sq.x + lo;            // global index of chunk lo
     const long long slot0 = ra.span ? (long long)n * ra.span : first;
+    const size_t seg_off = (size_t)seg * sc.nc * 128 * 128;  // (seg, chain 0) in a [P][nc][K][V] buffer
     const float* s_in = lo == 0 ? s0 : ra.carry;
     float* s_out = hi == seq_chunks ? sN : ra.carry;
+    bool s_identity = false, zero_u = false;
+    if (sc.mode == 1) {
+        s_in = nullptr;
+        s_identity = zero_u = var == 1;
+        s_out = sc.summ + (size_t)var * sc.P * sc.nc * 128 * 128 + seg_off;
+        o = nullptr;
+    } else if (sc.mode == 2) {
+        s_in = seg == 0 ? s0 : sc.starts + seg_off;
+        s_out = hi == seq_chunks ? sN : nullptr;
+    }
     auto rec_of = [&](int ci) {
         return records + ((size_t)(slot0 + ci) * H + h) * TcRecord::bytes;
     };
@@ -901,15 +927,17 @@ __device__ __forceinline__ void ho_chain(int n, int h, const int* __restrict__ f
                 break;
             tc_fence_after();
             const int4 ent = cx.chunk(first + ci);
-            __nv_bfloat16* dst = o + ((size_t)ent.y * H + h) * 128 + v;
+            if (o) {
+                __nv_bfloat16* dst = o + ((size_t)ent.y * H + h) * 128 + v;
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                float ov[32];
-                tmem_ld32(tmem_addr(tmem + kColD1 + 128 * (ci & 1) + 64 + 32 * hh, qd, 0), ov);
+                for (int hh = 0; hh < 2; ++hh) {
+                    float ov[32];
+                    tmem_ld32(tmem_addr(tmem + kColD1 + 128 * (ci & 1) + 64 + 32 * hh, qd, 0), ov);
 #pragma unroll
-                for (int x = 0; x < 32; ++x) {
-                    const int i = 32 * hh + x;
-                    if (i < ent.z) dst[(size_t)i * H * 128] = __float2bfloat16_rn(ov[x]);
+                    for (int x = 0; x < 32; ++x) {
+                        const int i = 32 * hh + x;
+                        if (i < ent.z) dst[(size_t)i * H * 128] = __float2bfloat16_rn(ov[x]);
+                    }
                 }
             }
             tc_fence_before();
@@ -990,7 +1018,8 @@ __device__ __forceinline__ void ho_chain(int n, int h, const int* __restrict__ f
         const size_t st_base = ((size_t)n * H + h) * 128 * 128 + (size_t)(64 * half) * 128 + v;
         float S[64];
 #pragma unroll
-        for (int x = 0; x < 64; ++x) S[x] = s_in ? s_in[st_base + (size_t)x * 128] : 0.f;
+        for (int x = 0; x < 64; ++x)
+            S[x] = s_in ? s_in[st_base + (size_t)x * 128] : (s_identity && 64 * half + x == v ? 1.f : 0.f);
         // S^T as bf16 operand columns (2 keys per column) of this thread's lane
         auto write_state = [&]() {
 #pragma unroll
@@ -1026,7 +1055,7 @@ __device__ __forceinline__ void ho_chain(int n, int h, const int* __restrict__ f
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
                     float uf[8];
-                    unpack8(ur[q4], uf);
+                    unpack8(zero_u ? make_uint4(0u, 0u, 0u, 0u) : ur[q4], uf);
 #pragma unroll
                     for (int m = 0; m < 4; ++m)
                         pk[4 * q4 + m] = pack_bf16x2(uf[2 * m] - ws[8 * q4 + 2 * m],
@@ -1079,6 +1108,53 @@ kda_h_o_tc(const uint8_t* __restrict__ records, ChunkIndex cx, long long max_chu
            const float* __restrict__ s0, __nv_bfloat16* __restrict__ o, float* __restrict__ sN,
            int H, int* __restrict__ status) {
     ho_chain<false>(blockIdx.x / H, blockIdx.x % H, nullptr, records, cx, max_chunks, ra, s0, o, sN, H, status);
+}
+
+// Scan passes of the per-chain recurrence: block b = (var * P + seg) * nc + chain (mode 1)
+// or seg * nc + chain (mode 2).
+__global__ void __launch_bounds__(kHoThreads, 1)
+kda_h_o_scan(const uint8_t* __restrict__ records, ChunkIndex cx, long long max_chunks, ScanArgs sc,
+             const float* __restrict__ s0, __nv_bfloat16* __restrict__ o, float* __restrict__ sN,
+             int H, int* __restrict__ status) {
+    const int chain = (int)(blockIdx.x % sc.nc), rest = (int)(blockIdx.x / sc.nc);
+    ho_chain<false>(chain / H, chain % H, nullptr, records, cx, max_chunks, RangeArgs{}, s0, o, sN, H,
+                    status, sc, rest % sc.P, rest / sc.P);
+}
+
+// Segment start states of the scan: X_0 = S_0 (or 0), X_{s+1} = Phi_s X_s + Psi_s, in fp32
+// (plain CUDA-core products; P - 1 dependent steps per chain).  Block (chain, 32-column
+// slice of V), 256 threads: thread (row r = t / 2, columns 16 (t % 2) ..) of the slice.
+constexpr int kMergeThreads = 256;
+__global__ void __launch_bounds__(kMergeThreads)
+kda_scan_merge(ScanArgs sc, const float* __restrict__ s0, float* __restrict__ starts) {
+    __shared__ float X[128][32];
+    const int chain = blockIdx.x, c0 = 32 * blockIdx.y;
+    const int t = threadIdx.x, r = t >> 1, cc = 16 * (t & 1);
+    const size_t cst = (size_t)chain * 128 * 128;
+    const size_t plane = (size_t)sc.nc * 128 * 128;
+    for (int x = 0; x < 16; ++x)
+        X[r][cc + x] = s0 ? s0[cst + (size_t)r * 128 + c0 + cc + x] : 0.f;
+    __syncthreads();
+    for (int sg = 0; sg + 1 < sc.P; ++sg) {
+        const float* phi = sc.summ + (size_t)(sc.P + sg) * plane + cst + (size_t)r * 128;
+        const float* psi = sc.summ + (size_t)sg * plane + cst + (size_t)r * 128 + c0 + cc;
+        float acc[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x) acc[x] = psi[x];
+        for (int d = 0; d < 128; ++d) {
+            const float f = phi[d];
+#pragma unroll
+            for (int x = 0; x < 16; ++x) acc[x] = fmaf(f, X[d][cc + x], acc[x]);
+        }
+        __syncthreads();
+        float* dst = starts + (size_t)(sg + 1) * plane + cst + (size_t)r * 128 + c0 + cc;
+#pragma unroll
+        for (int x = 0; x < 16; ++x) {
+            X[r][cc + x] = acc[x];
+            dst[x] = acc[x];
+        }
+        __syncthreads();
+    }
 }
 
 // Fused schedule for few chains of fixed-length sequences: one persistent CTA per SM.
@@ -1547,6 +1623,38 @@ cudaError_t launch_tc(const void* q, const void* k, const void* v, const float* 
         cudaFuncSetAttribute(intra, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kIntraSmem);
     cudaFuncSetAttribute(ho, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ho_smem);
     __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(o);
+
+    // Scan schedule: the intra-chunk kernel (per-chain records), the segment summaries,
+    // their merge, and the replay of every segment from its merged start state.
+    if (L.scan && !ev) {
+        auto* ik = opts ? kda_intra_tc<true, TcRecord> : kda_intra_tc<false, TcRecord>;
+        if (cudaError_t e = cudaFuncSetAttribute(ik, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)kIntraSmem))
+            return e;
+        if (cudaError_t e = cudaFuncSetAttribute(kda_h_o_scan, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)kHoSmem))
+            return e;
+        ik<<<(unsigned)(L.max_chunks * H), kIntraThreads, kIntraSmem, s>>>(
+            tq, tk, tv, tg, beta, scale, ga, H, cx, L.max_chunks, RangeArgs{}, records, status);
+        if (cudaError_t e = cudaGetLastError()) return e;
+        ScanArgs sc;
+        sc.P = L.scan_P;
+        sc.L = L.scan_L;
+        sc.nc = L.N * H;
+        sc.summ = reinterpret_cast<float*>(ws + L.summ_off);
+        sc.starts = reinterpret_cast<const float*>(ws + L.starts_off);
+        sc.mode = 1;
+        kda_h_o_scan<<<(unsigned)(2 * sc.P * sc.nc), kHoThreads, kHoSmem, s>>>(records, cx, L.max_chunks, sc,
+                                                                             s0, ob, sN, H, status);
+        if (cudaError_t e = cudaGetLastError()) return e;
+        kda_scan_merge<<<dim3((unsigned)sc.nc, 4), kMergeThreads, 0, s>>>(
+            sc, s0, reinterpret_cast<float*>(ws + L.starts_off));
+        if (cudaError_t e = cudaGetLastError()) return e;
+        sc.mode = 2;
+        kda_h_o_scan<<<(unsigned)(sc.P * sc.nc), kHoThreads, kHoSmem, s>>>(records, cx, L.max_chunks, sc,
+                                                                         s0, ob, sN, H, status);
+        return cudaGetLastError();
+    }
 
     // Fused schedule: one cooperative launch, one CTA per SM (the recurrence CTAs poll
     // flags the other CTAs set, so all CTAs must be resident); the flags start cleared.

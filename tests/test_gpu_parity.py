@@ -200,6 +200,36 @@ def test_fused_schedule(kda, orc, shape, monkeypatch):
     assert torch.equal(o_2, o_f) and torch.equal(f_2, f_f)
 
 
+@pytest.mark.parametrize("shape", [(1, 64 * 40 + 17, 2, 0.1), (2, 64 * 9, 3, None), (1, 64 * 4, 1, 0.1)],
+                         ids=["tail_init", "batch2", "four_chunks"])
+def test_scan_schedule(kda, orc, shape, monkeypatch):
+    """The chunk-parallel scan (segment summaries Phi, Psi from S = I with U = 0 and from
+    S = 0, a per-chain fp32 merge, then every segment replayed from its merged start)
+    matches the oracle and the two-kernel schedule to the bf16 tolerance."""
+    B, T, H, init = shape
+    inp = make_inputs(custom(B=B, T=T, H=H, K=128, V=128, dtype=torch.bfloat16,
+                             init_std=init, seed=T * 3 + H), device="cuda")
+    monkeypatch.setenv("KDA_SCHEDULE", "scan")
+    assert kda.launch_count(B, T, H, 128, 128) == 4   # intra, summaries, merge, replay
+    o_s, f_s = run_gpu(kda, inp)
+    monkeypatch.setenv("KDA_SCHEDULE", "two")
+    o_t, f_t = run_gpu(kda, inp)
+    monkeypatch.delenv("KDA_SCHEDULE")
+    o_ref, f_ref = run_oracle(orc, inp)
+    for o_x, f_x in ((o_s, f_s), (o_t, f_t)):
+        eo, ef = errors(o_x, f_x, o_ref, f_ref)
+        assert eo <= 2e-2 and ef <= 2e-2, (eo, ef)
+    assert (o_s.float() - o_t.float()).abs().max().item() <= 2e-2
+
+
+def test_scan_schedule_automatic(kda, orc):
+    """Two chains of 128 chunks take the scan schedule by themselves."""
+    inp = make_inputs(custom(B=1, T=64 * 128, H=2, K=128, V=128, dtype=torch.bfloat16,
+                             init_std=0.1, seed=77), device="cuda")
+    assert kda.launch_count(1, 64 * 128, 2, 128, 128) == 4
+    check(kda, orc, inp)
+
+
 @pytest.mark.parametrize("mode", ["two", "fused"])
 def test_forced_schedules_dense(kda, orc, mode, monkeypatch):
     """The dense workload's shape under each schedule, checked on a sample of chains."""
