@@ -137,7 +137,10 @@ size_t kda_fwd_workspace_bytes(int B, int T, int H, int K, int V, int num_seqs,
  *              events it needs; no device memory is allocated).  The second stream forks
  *              from and joins back into `stream` through events, so the call stays ordered
  *              on `stream` and can be captured into a CUDA graph.
- * The environment variable KDA_SCHEDULE ("two", "pipelined", "fused") forces a schedule
+ *   scan       at most an eighth of the SMs' count of chains and at least 128 chunks per
+ *              sequence: chunk-parallel state scan (segment summaries, a per-chain merge of
+ *              segment start states, then every segment replayed): four launches.
+ * The environment variable KDA_SCHEDULE ("two", "pipelined", "fused", "scan") forces a schedule
  * where the sizes allow it (read at workspace sizing and at each call, which must agree).
  * kda_fwd_launch_count gives the number of kernel launches. */
 kda_status kda_fwd(const void* q, const void* k, const void* v, const float* g,
@@ -257,7 +260,7 @@ kda_status kda_selftest_umma(const void* A, const void* B, float* D, int N, int 
 /* Number of kernel launches kda_fwd makes for these sizes on the current device: the
  * chunk-index kernel (packed input, and the fp32 / other-shape path), the intra-chunk
  * kernel and the recurrence kernel (pipelined calls launch the last two once per chunk
- * range; fused calls make one launch); -1 for sizes kda_fwd rejects. */
+ * range; fused calls make one launch, scan calls four); -1 for sizes kda_fwd rejects. */
 int kda_fwd_launch_count(int B, int T, int H, int K, int V, int num_seqs, int chunk_size,
                          kda_dtype dtype);
 

@@ -75,6 +75,11 @@ class Oracle:
         self.lib.kda_oracle_gate.restype = ctypes.c_int
         self.lib.kda_oracle_l2norm.argtypes = [dp, ctypes.c_long, ctypes.c_int, ctypes.c_double, dp]
         self.lib.kda_oracle_l2norm.restype = ctypes.c_int
+        self.lib.kda_oracle_chunk_summaries.argtypes = [dp, dp, dp, dp, dp, ctypes.c_double,
+                                                        ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                        ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                        dp, dp, ctypes.c_int]
+        self.lib.kda_oracle_chunk_summaries.restype = ctypes.c_int
         self.threads_used = 0
 
     def gate(self, x, a_log, dt_bias=None, lower_bound=0.0):
@@ -143,6 +148,52 @@ class Oracle:
             raise ValueError(f"kda_oracle_chunkwise failed with code {rc}")
         self.threads_used = rc
         return o, fin
+
+    def chunk_summaries(self, q, k, v, g, beta, scale, chunk_size: int = 64,
+                        num_threads: int = 0):
+        """Affine summary of every chunk of fixed-length input (Tokamax design doc,
+        context-parallel section): chunk j maps its start state S to Phi_j S + Psi_j.
+        Returns (phi [B,H,nct,K,K], psi [B,H,nct,K,V]) in fp64."""
+        q, k, v, g, beta = (_f64(t) for t in (q, k, v, g, beta))
+        B, T, H, K = q.shape
+        V = v.shape[-1]
+        nct = -(-T // chunk_size)
+        phi = np.empty((B, H, nct, K, K), dtype=np.float64)
+        psi = np.empty((B, H, nct, K, V), dtype=np.float64)
+        rc = self.lib.kda_oracle_chunk_summaries(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), B, T, H, K, V,
+            int(chunk_size), _ptr(phi), _ptr(psi), int(num_threads))
+        if rc < 0:
+            raise ValueError(f"kda_oracle_chunk_summaries failed with code {rc}")
+        self.threads_used = rc
+        return phi, psi
+
+
+def compose_summaries(phi, psi, lo: int, hi: int):
+    """Summary of chunks lo .. hi-1 taken in order, from the per-chunk summaries
+    [..., nct, K, K] / [..., nct, K, V]: applying chunk a then chunk b gives
+    (Phi_b Phi_a, Phi_b Psi_a + Psi_b) (Tokamax design doc, context-parallel section)."""
+    K = phi.shape[-1]
+    P = np.broadcast_to(np.eye(K), phi.shape[:-3] + (K, K)).copy()
+    Q = np.zeros(psi.shape[:-3] + psi.shape[-2:])
+    for j in range(lo, hi):
+        P = phi[..., j, :, :] @ P
+        Q = phi[..., j, :, :] @ Q + psi[..., j, :, :]
+    return P, Q
+
+
+def segment_start_states(phi, psi, initial_state, segment_chunks: int):
+    """Start states of the segments of `segment_chunks` chunks, merged in order from the
+    segments' composed summaries: X_0 = S_0, X_{s+1} = Phi_s X_s + Psi_s.  Returns
+    [..., n_segments, K, V] and the state after the last segment."""
+    nct = phi.shape[-3]
+    X = np.zeros(psi.shape[:-3] + psi.shape[-2:]) if initial_state is None else _f64(initial_state).copy()
+    starts = []
+    for lo in range(0, nct, segment_chunks):
+        starts.append(X.copy())
+        P, Q = compose_summaries(phi, psi, lo, min(lo + segment_chunks, nct))
+        X = P @ X + Q
+    return np.stack(starts, axis=-3), X
 
 
 _DEFAULT: Optional[Oracle] = None

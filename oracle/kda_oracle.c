@@ -287,6 +287,55 @@ static int chunkwise_unit(const oracle_job* J, int n, int h) {
 }
 
 /* ------------------------------------------------------------------------- */
+/* Affine chunk summaries ([TKD] context-parallel section: each chunk maps its */
+/* start state affinely, S' = Phi S + Psi)                                    */
+/* ------------------------------------------------------------------------- */
+
+/* The summary job reuses oracle_job: o points at a scratch output the chunk steps may
+ * overwrite, final_state at Phi [N][H][nct][K][K] and initial_state at Psi
+ * [N][H][nct][K][V] (both written; cast away const for Psi). */
+static int summary_unit(const oracle_job* J, int n, int h) {
+    const int K = J->K, V = J->V;
+    chunk_scratch s;
+    if (alloc_scratch(&s, J->C, K, V)) return -2;
+    double* S = (double*)malloc((size_t)K * V * sizeof(double));
+    if (!S) {
+        free_scratch(&s);
+        return -2;
+    }
+    long t0, t1;
+    seq_range(J, n, &t0, &t1);
+    const long nct = ((long)J->T + J->C - 1) / J->C;
+    double* Phi = J->final_state;
+    double* Psi = (double*)J->initial_state;
+    long j = 0;
+    for (long c0 = t0; c0 < t1; c0 += J->C, ++j) {
+        const int c = (int)((t1 - c0) < J->C ? (t1 - c0) : J->C);
+        /* the chunk's W, U, K_bar and G do not depend on the state it starts from */
+        memset(S, 0, (size_t)K * V * sizeof(double));
+        chunk_step(J, h, c0, c, S, &s);
+        double* phi = Phi + (((size_t)n * J->H + h) * nct + j) * K * K;
+        double* psi = Psi + (((size_t)n * J->H + h) * nct + j) * K * V;
+        /* Phi = Diag(gamma^C) - K_bar^T W;  Psi = K_bar^T U  (gamma^C = 2^{G^{C-1}}) */
+        for (int d = 0; d < K; ++d) {
+            for (int e = 0; e < K; ++e) {
+                double acc = 0.0;
+                for (int r = 0; r < c; ++r) acc += s.Kbar[(size_t)r * K + d] * s.W[(size_t)r * K + e];
+                phi[(size_t)d * K + e] = (d == e ? exp2(s.G[(size_t)(c - 1) * K + d]) : 0.0) - acc;
+            }
+            for (int jv = 0; jv < V; ++jv) {
+                double acc = 0.0;
+                for (int r = 0; r < c; ++r) acc += s.Kbar[(size_t)r * K + d] * s.U[(size_t)r * V + jv];
+                psi[(size_t)d * V + jv] = acc;
+            }
+        }
+    }
+    free(S);
+    free_scratch(&s);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------- */
 /* Threading and argument checks                                              */
 /* ------------------------------------------------------------------------- */
 
@@ -374,6 +423,21 @@ int kda_oracle_recurrent(const double* q, const double* k, const double* v,
                  1, o, final_state))
         return -1;
     return run(&J, recurrent_unit, num_threads);
+}
+
+int kda_oracle_chunk_summaries(const double* q, const double* k, const double* v,
+                               const double* g, const double* beta, double scale, int B, int T,
+                               int H, int K, int V, int chunk_size, double* phi, double* psi,
+                               int num_threads) {
+    oracle_job J;
+    if (!phi || !psi) return -1;
+    double* o_scratch = (double*)malloc(((size_t)B * T * H * V + 1) * sizeof(double));
+    if (!o_scratch) return -2;
+    const int rc = fill_job(&J, q, k, v, g, beta, scale, psi, NULL, 0, B, T, H, K, V, chunk_size,
+                            o_scratch, phi);
+    int out = rc ? -1 : run(&J, summary_unit, num_threads);
+    free(o_scratch);
+    return out;
 }
 
 int kda_oracle_chunkwise(const double* q, const double* k, const double* v,

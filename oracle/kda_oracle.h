@@ -63,6 +63,15 @@ int kda_oracle_chunkwise(const double* q, const double* k, const double* v,
  *   lower_bound == 0:  ell = -lambda_h * softplus(x'),  softplus(y) = ln(1 + e^y);
  *   otherwise:         ell = lower_bound * sigmoid(lambda_h x'),  sigmoid(y) = 1/(1+e^-y).
  * x and ell are [rows][H][K] (rows = B * T).  Returns 1, or -1 for invalid arguments. */
+/* Affine summary of every chunk of fixed-length input ([TKD] context-parallel section):
+ * the chunk maps its start state S to Phi S + Psi with Phi = Diag(gamma^C) - K_bar^T W
+ * (K x K) and Psi = K_bar^T U (K x V), W, U, K_bar and gamma^C as in the chunkwise form.
+ * phi: [B][H][nct][K][K], psi: [B][H][nct][K][V], nct = ceil(T / chunk_size). */
+int kda_oracle_chunk_summaries(const double* q, const double* k, const double* v,
+                               const double* g, const double* beta, double scale, int B, int T,
+                               int H, int K, int V, int chunk_size, double* phi, double* psi,
+                               int num_threads);
+
 int kda_oracle_gate(const double* x, const double* a_log, const double* dt_bias,
                     double lower_bound, long rows, int H, int K, double* ell);
 

@@ -345,6 +345,54 @@ def pin_l2norm(oracle):
     assert np.allclose(oracle.l2norm(tiny), [[3e-2, 4e-2], [0.0, 0.0]], rtol=1e-14, atol=0)
 
 
+# ---------------------------------------------------------------------------
+# Affine chunk summaries (Tokamax design doc, context-parallel section)
+# ---------------------------------------------------------------------------
+
+def pin_affine_summaries_replay(oracle):
+    """Each chunk maps its start state affinely (S' = Phi S + Psi): composing the chunk
+    summaries in order and applying them to S_0 reaches the token recurrence's final
+    state, and the merged segment start states are the recurrence's states at the
+    segment boundaries (prefixes of the sequence)."""
+    from oracle import compose_summaries, segment_start_states
+    rng = np.random.default_rng(21)
+    B, T, H, K, V, C = 2, 157, 2, 16, 12, 16
+    q, k, v, g, beta = _rand_inputs(rng, B, T, H, K, V, g_max=0.8)
+    s0 = rng.standard_normal((B, H, K, V))
+    scale = 0.3
+    phi, psi = oracle.chunk_summaries(q, k, v, g, beta, scale, chunk_size=C)
+    nct = -(-T // C)
+    assert phi.shape == (B, H, nct, K, K) and psi.shape == (B, H, nct, K, V)
+    Pall, Qall = compose_summaries(phi, psi, 0, nct)
+    _, fin = oracle.recurrent(q, k, v, g, beta, scale, initial_state=s0)
+    assert np.allclose(Pall @ s0 + Qall, fin, rtol=0, atol=1e-10), "summaries do not replay the recurrence"
+    seg = 3
+    starts, last = segment_start_states(phi, psi, s0, seg)
+    assert np.allclose(last, fin, rtol=0, atol=1e-10)
+    for si in range(1, starts.shape[-3]):
+        t_end = si * seg * C
+        _, fin_p = oracle.recurrent(q[:, :t_end], k[:, :t_end], v[:, :t_end], g[:, :t_end],
+                                    beta[:, :t_end], scale, initial_state=s0)
+        assert np.allclose(starts[..., si, :, :], fin_p, rtol=0, atol=1e-10), f"segment {si} start"
+
+
+def pin_affine_beta_zero(oracle):
+    """With beta = 0 no chunk writes: Phi_j = Diag(exp(sum of g over chunk j)) and
+    Psi_j = 0 (Eq. (1) with beta_t = 0)."""
+    rng = np.random.default_rng(22)
+    B, T, H, K, V, C = 1, 50, 2, 8, 6, 16
+    q, k, v, g, _ = _rand_inputs(rng, B, T, H, K, V, g_max=0.5)
+    beta = np.zeros((B, T, H))
+    phi, psi = oracle.chunk_summaries(q, k, v, g, beta, 0.5, chunk_size=C)
+    for j in range(-(-T // C)):
+        gam = np.exp(g[:, j * C:(j + 1) * C].sum(axis=1))       # [B,H,K]
+        ref = np.zeros((B, H, K, K))
+        for d in range(K):
+            ref[..., d, d] = gam[..., d]
+        assert np.allclose(phi[:, :, j], ref, rtol=1e-13, atol=1e-15), f"Phi of chunk {j}"
+        assert np.array_equal(psi[:, :, j], np.zeros((B, H, K, V))), f"Psi of chunk {j}"
+
+
 ALL_PINS = [
     pin_eq1_exact_rational,
     pin_linear_attention,
@@ -357,4 +405,6 @@ ALL_PINS = [
     pin_gate_softplus,
     pin_gate_sigmoid,
     pin_l2norm,
+    pin_affine_summaries_replay,
+    pin_affine_beta_zero,
 ]

@@ -58,6 +58,15 @@ MUTANTS = {
                         "acc += s->A[(size_t)r * c + j] * V_(j, jv);")],
     "Kbar_from_chunk_start": [("K_(r, d) * exp2(G_(c - 1, d) - G_(r, d))",
                                "K_(r, d) * exp2(-G_(r, d))")],
+    # affine chunk summaries
+    "phi_plus": [("d == e ? exp2(s.G[(size_t)(c - 1) * K + d]) : 0.0) - acc;",
+                  "d == e ? exp2(s.G[(size_t)(c - 1) * K + d]) : 0.0) + acc;")],
+    "phi_transposed": [("acc += s.Kbar[(size_t)r * K + d] * s.W[(size_t)r * K + e];",
+                        "acc += s.Kbar[(size_t)r * K + e] * s.W[(size_t)r * K + d];")],
+    "phi_gamma_first_row": [("(d == e ? exp2(s.G[(size_t)(c - 1) * K + d]) : 0.0)",
+                             "(d == e ? exp2(s.G[d]) : 0.0)")],
+    "psi_without_kbar": [("acc += s.Kbar[(size_t)r * K + d] * s.U[(size_t)r * V + jv];",
+                          "acc += s.U[(size_t)r * V + jv];")],
     "Vnew_sign": [("s->U[(size_t)r * V + jv] - acc;", "s->U[(size_t)r * V + jv] + acc;")],
     "O_without_inter": [("orow[jv] = inter + intra;", "orow[jv] = intra;")],
     "inter_without_gate": [("J->scale * Q_(r, d) * exp2(G_(r, d)) * S[(size_t)d * V + jv]",
