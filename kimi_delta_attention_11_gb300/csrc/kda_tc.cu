@@ -151,6 +151,9 @@ constexpr size_t kIntraSmem = IntraMap::END + 1024;  // + alignment slack
 // Row strides (floats) of the solve's fp32 tiles, chosen so that the fragment loads of
 // the 16x16 block products hit distinct banks.
 constexpr int kLs = 72, kBs = 20;
+// The thread that issues (and, for published records, completes) the record's bulk stores:
+// lane 0 of the last warp, which is idle in the solve stage where the completion is waited.
+constexpr int kStoreThread = kIntraThreads - 32;
 static_assert(IntraMap::LF + 64 * kLs * 4 <= IntraMap::RA + 32768, "L tile overflows");
 static_assert(IntraMap::JB + 6 * 16 * kBs * 4 <= IntraMap::AIA, "J blocks overflow");
 static_assert(4 * 16 * kBs * 4 <= IntraMap::END - IntraMap::MISC, "X blocks overflow");
@@ -230,14 +233,6 @@ __device__ __forceinline__ bool intra_unit(const CUtensorMap* tmq, const CUtenso
             tma_load_2d(sm + M::VT + pp * 8192, tmv, h * 128 + 64 * pp, t0, &bar_tma);
         }
         tma_load_2d(sm + M::RA, tmg, h * 128, t0, &bar_tma);
-        // the previous record of this lane is published while the tiles load: its bulk
-        // stores complete, then its flag is set with release semantics
-        if (prev_flag) {
-            bulk_wait_all();
-            fence_proxy_async_global();
-            __threadfence();
-            st_release_gpu(prev_flag, 1);
-        }
     }
     if (tid < 64) betas[tid] = tid < len ? beta[(size_t)(t0 + tid) * H + h] : 0.f;
     mbar_wait_abortable(&bar_tma, k & 1u, status, abort_flag);
@@ -581,6 +576,15 @@ __device__ __forceinline__ bool intra_unit(const CUtensorMap* tmq, const CUtenso
         lane_sync();
         // Stage 3 (warps 0-2): X20 = J21 J10 - J20, X31 = J32 J21 - J31,
         // X30 = J31 J10 + J32 J20 - J30 - J32 (J21 J10) (warp 2, through a scratch block).
+        // The previous record of this lane is published by the thread that stored it
+        // (warp 7, idle in this stage): its bulk stores, long complete, are waited for,
+        // then the flag is set with release semantics.
+        if (prev_flag && tid == kStoreThread) {
+            bulk_wait_all();
+            fence_proxy_async_global();
+            __threadfence();
+            st_release_gpu(prev_flag, 1);
+        }
         if (warp < 3) {
             float acc[2][4];
             const float* J = JB;
@@ -654,11 +658,10 @@ __device__ __forceinline__ bool intra_unit(const CUtensorMap* tmq, const CUtenso
                            desc_sw128(sb + M::AIA + kk * 32), id_u, kk > 0 ? 1u : 0u);
         }
         mma_commit_w(&bar_wu);
-        if (lane == 0) {
-            bulk_store(rec + Rec::aqk, sm + M::AQS, 8192);
-            bulk_commit();
-        }
-        __syncwarp();
+    }
+    if (tid == kStoreThread) {
+        bulk_store(rec + Rec::aqk, sm + M::AQS, 8192);
+        bulk_commit();
     }
     mbar_wait_abortable(&bar_wu, k & 1u, status, abort_flag);
     tc_fence_after();
@@ -701,7 +704,7 @@ __device__ __forceinline__ bool intra_unit(const CUtensorMap* tmq, const CUtenso
     fence_proxy_async_smem();
     tc_fence_before();
     lane_sync();
-    if (tid == 0) {
+    if (tid == kStoreThread) {
         bulk_store(rec + Rec::wq, sm + M::WST, 8192);
         bulk_store(rec + Rec::wq + 16384, sm + M::WST + 8192, 8192);
         if constexpr (Rec::sliced) {
@@ -712,7 +715,7 @@ __device__ __forceinline__ bool intra_unit(const CUtensorMap* tmq, const CUtenso
         }
         bulk_commit();
         // only the shared-memory sources must outlive the copies here; a record that is
-        // published is waited for when the next one's tiles load (or after the last)
+        // published is waited for during the next one's solve (or after the last)
         bulk_wait_read_all();
     }
     // A published record's direct stores (query and key rows, gamma) by every thread are
@@ -1227,7 +1230,7 @@ __device__ __forceinline__ void intra_lane(const FusedArgs& A, uint8_t* sm, uint
                                              prev, true, sm, tmem, lid, tid_u, k, A.status);
         if (!ok) break;
     }
-    if (ok && k > 0 && tid == 0) {  // the lane's last record
+    if (ok && k > 0 && tid == kStoreThread) {  // the lane's last record (its storing thread)
         const long long ul = u0 + (long long)(k - 1) * lanes;
         bulk_wait_all();
         fence_proxy_async_global();
