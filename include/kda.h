@@ -264,6 +264,17 @@ kda_status kda_selftest_umma(const void* A, const void* B, float* D, int N, int 
 int kda_fwd_launch_count(int B, int T, int H, int K, int V, int num_seqs, int chunk_size,
                          kda_dtype dtype);
 
+/* Schedule kda_fwd takes for these sizes on the current device (see kda_fwd), or -1 for
+ * sizes kda_fwd rejects.  kda_fwd_profiled always runs the two-kernel schedule. */
+typedef enum {
+    KDA_SCHEDULE_TWO_KERNELS = 0,
+    KDA_SCHEDULE_PIPELINED = 1,
+    KDA_SCHEDULE_FUSED = 2,
+    KDA_SCHEDULE_SCAN = 3
+} kda_schedule;
+int kda_fwd_schedule(int B, int T, int H, int K, int V, int num_seqs, int chunk_size,
+                     kda_dtype dtype);
+
 /* Version of this ABI (major * 100 + minor). */
 int kda_abi_version(void);
 

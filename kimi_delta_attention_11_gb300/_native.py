@@ -65,6 +65,7 @@ _SIGNATURES = {
     "kda_get_device_status": (_i, [_vp, _vp]),
     "kda_abi_version": (_i, []),
     "kda_fwd_launch_count": (_i, [_i, _i, _i, _i, _i, _i, _i, _i]),
+    "kda_fwd_schedule": (_i, [_i, _i, _i, _i, _i, _i, _i, _i]),
 }
 
 
@@ -124,6 +125,18 @@ def launch_count(B: int, T: int, H: int, K: int, V: int, num_seqs: int = 0,
     if n < 0:
         raise KdaError(1, "kda_fwd_launch_count")
     return int(n)
+
+
+SCHEDULES = {0: "two_kernels", 1: "pipelined", 2: "fused", 3: "scan"}
+
+
+def schedule(B: int, T: int, H: int, K: int, V: int, num_seqs: int = 0,
+             dtype: torch.dtype = torch.bfloat16, chunk_size: int = 64) -> str:
+    """Schedule one kda_fwd takes for these sizes on the current device."""
+    n = load_library().kda_fwd_schedule(B, T, H, K, V, num_seqs, chunk_size, DTYPE_CODES[dtype])
+    if n < 0:
+        raise KdaError(1, "kda_fwd_schedule")
+    return SCHEDULES[int(n)]
 
 
 def _gate_struct(gate: Optional[dict], H: int, K: int):

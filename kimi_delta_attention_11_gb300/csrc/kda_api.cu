@@ -154,7 +154,18 @@ kda_status check_device() {
 
 extern "C" {
 
-int kda_abi_version(void) { return 101; }
+int kda_abi_version(void) { return 102; }
+
+int kda_fwd_schedule(int B, int T, int H, int K, int V, int num_seqs, int chunk_size,
+                     kda_dtype dtype) {
+    const bool packed = num_seqs > 0;
+    if (check_sizes(B, T, H, K, V, num_seqs, packed, chunk_size, dtype) != KDA_OK) return -1;
+    const Layout L = make_layout(B, T, H, K, V, num_seqs, packed, dtype);
+    if (L.fused) return KDA_SCHEDULE_FUSED;
+    if (L.scan) return KDA_SCHEDULE_SCAN;
+    if (L.span > 0) return KDA_SCHEDULE_PIPELINED;
+    return KDA_SCHEDULE_TWO_KERNELS;
+}
 
 int kda_fwd_launch_count(int B, int T, int H, int K, int V, int num_seqs, int chunk_size,
                          kda_dtype dtype) {

@@ -38,13 +38,14 @@ def test_status_strings(lib):
     for s in range(8):
         assert lib.kda_status_string(s).decode()
     assert lib.kda_status_string(99).decode() == "unknown status"
-    assert lib.kda_abi_version() == 101
+    assert lib.kda_abi_version() == 102
 
 
 def test_launch_count(lib):
     """bf16 K = V = 128 fixed length: no index kernel, intra + recurrence (once per range
     of 32 chunks when pipelined: <= 128 chains, >= 512 chunks per sequence); packed input
-    and the other paths: index + intra + recurrence."""
+    and the other paths: index + intra + recurrence.  (Without a device the SM count is
+    unknown, so no call is fused or scanned; tests/test_gpu_parity.py covers those.)"""
     lc = lambda *a: lib.kda_fwd_launch_count(*a)
     bf16, f32 = 0, 1
     assert lc(2, 4096, 16, 128, 128, 0, 64, bf16) == 2             # 64 chunks
@@ -57,6 +58,17 @@ def test_launch_count(lib):
     assert lc(1, 131072, 32, 128, 128, 0, 64, f32) == 3            # fp32 path
     assert lc(1, 131072, 32, 64, 64, 0, 64, bf16) == 3             # other shapes
     assert lc(2, 4096, 16, 128, 128, 0, 32, bf16) == -1            # rejected sizes
+
+
+def test_schedule_query(lib):
+    """kda_fwd_schedule names the schedule kda_fwd_launch_count counts."""
+    sc = lambda *a: lib.kda_fwd_schedule(*a)
+    bf16, f32 = 0, 1
+    assert sc(1, 131072, 32, 128, 128, 0, 64, bf16) == 1            # pipelined
+    assert sc(32, 2048, 32, 128, 128, 0, 64, bf16) == 0             # two kernels
+    assert sc(1, 37000, 32, 128, 128, 8, 64, bf16) == 0             # packed
+    assert sc(1, 131072, 32, 128, 128, 0, 64, f32) == 0             # fp32 path
+    assert sc(2, 4096, 16, 128, 128, 0, 32, bf16) == -1             # rejected sizes
 
 
 def test_workspace_bytes_rules(lib):

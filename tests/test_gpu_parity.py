@@ -223,10 +223,15 @@ def test_scan_schedule(kda, orc, shape, monkeypatch):
 
 
 def test_scan_schedule_automatic(kda, orc):
-    """Two chains of 128 chunks take the scan schedule by themselves."""
+    """Two chains of 128 chunks take the scan schedule by themselves; the plan's
+    workloads take theirs."""
     inp = make_inputs(custom(B=1, T=64 * 128, H=2, K=128, V=128, dtype=torch.bfloat16,
                              init_std=0.1, seed=77), device="cuda")
     assert kda.launch_count(1, 64 * 128, 2, 128, 128) == 4
+    assert kda.schedule(1, 64 * 128, 2, 128, 128) == "scan"
+    assert kda.schedule(2, 4096, 16, 128, 128) == "fused"           # dense
+    assert kda.schedule(1, 131072, 32, 128, 128) == "fused"         # long
+    assert kda.schedule(32, 2048, 32, 128, 128) == "two_kernels"    # serving
     check(kda, orc, inp)
 
 
@@ -343,6 +348,7 @@ SAMPLES = {
     "varlen_bf16": (None, [0, 13, 31]),
     "long_bf16": (None, [0, 21]),
     "serving_bf16": ([0, 17, 31], [0, 9, 31]),
+    "few_long_bf16": (None, [1]),
 }
 
 

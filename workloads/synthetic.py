@@ -42,7 +42,8 @@ class Workload:
         return {torch.bfloat16: "bf16", torch.float32: "f32"}[self.dtype]
 
 
-# The five workloads of the KDA forward measurement plan (sizes and distributions).
+# The five workloads of the KDA forward measurement plan (sizes and distributions), and
+# one for the scan schedule.
 WORKLOADS: Dict[str, Workload] = {
     "tiny_f32": Workload("tiny_f32", B=1, T=256, H=2, K=64, V=64, dtype=torch.float32,
                          seed=1001),
@@ -55,6 +56,10 @@ WORKLOADS: Dict[str, Workload] = {
                           dtype=torch.bfloat16, g_max=0.5, init_std=0.1, seed=1004),
     "serving_bf16": Workload("serving_bf16", B=32, T=2048, H=32, K=128, V=128,
                              dtype=torch.bfloat16, beta_mean=2.0, seed=1005),
+    # Few, very long chains (the case the chunk-parallel state scan serves): 2 heads of
+    # one 262144-token sequence.
+    "few_long_bf16": Workload("few_long_bf16", B=1, T=262144, H=2, K=128, V=128,
+                              dtype=torch.bfloat16, g_max=0.5, init_std=0.1, seed=1007),
 }
 
 
