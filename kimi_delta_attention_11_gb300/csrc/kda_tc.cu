@@ -1125,40 +1125,67 @@ kda_h_o_scan(const uint8_t* __restrict__ records, ChunkIndex cx, long long max_c
 }
 
 // Segment start states of the scan: X_0 = S_0 (or 0), X_{s+1} = Phi_s X_s + Psi_s, in fp32
-// (plain CUDA-core products; P - 1 dependent steps per chain).  Block (chain, 32-column
-// slice of V), 256 threads: thread (row r = t / 2, columns 16 (t % 2) ..) of the slice.
+// (CUDA-core products; P - 1 dependent steps per chain).  Every column of X evolves on its
+// own, so block (chain, 8-column slice of V) carries its slice through all steps; 256
+// threads: thread (row r = t / 2, columns 4 (t % 2) ..) of the slice.  Phi_s is staged in
+// shared memory with rows padded to 129 floats (conflict-free reads down a column), and
+// the next step's Phi is loaded into registers while this step computes.
 constexpr int kMergeThreads = 256;
+constexpr int kMergeCols = 8;
 __global__ void __launch_bounds__(kMergeThreads)
 kda_scan_merge(ScanArgs sc, const float* __restrict__ s0, float* __restrict__ starts) {
-    __shared__ float X[128][32];
-    const int chain = blockIdx.x, c0 = 32 * blockIdx.y;
-    const int t = threadIdx.x, r = t >> 1, cc = 16 * (t & 1);
+    extern __shared__ float merge_smem[];
+    float* Phs = merge_smem;                 // [128][129]
+    float* X = merge_smem + 128 * 129;       // [128][kMergeCols]
+    const int chain = blockIdx.x, c0 = kMergeCols * blockIdx.y;
+    const int t = threadIdx.x, r = t >> 1, cc = 4 * (t & 1);
     const size_t cst = (size_t)chain * 128 * 128;
     const size_t plane = (size_t)sc.nc * 128 * 128;
-    for (int x = 0; x < 16; ++x)
-        X[r][cc + x] = s0 ? s0[cst + (size_t)r * 128 + c0 + cc + x] : 0.f;
-    __syncthreads();
+    for (int x = 0; x < 4; ++x)
+        X[r * kMergeCols + cc + x] = s0 ? s0[cst + (size_t)r * 128 + c0 + cc + x] : 0.f;
+    float4 ph[16];
+    auto load_phi = [&](int sg) {
+        const float4* src = reinterpret_cast<const float4*>(sc.summ + (size_t)(sc.P + sg) * plane + cst);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) ph[i] = src[t + kMergeThreads * i];
+    };
+    if (sc.P > 1) load_phi(0);
     for (int sg = 0; sg + 1 < sc.P; ++sg) {
-        const float* phi = sc.summ + (size_t)(sc.P + sg) * plane + cst + (size_t)r * 128;
-        const float* psi = sc.summ + (size_t)sg * plane + cst + (size_t)r * 128 + c0 + cc;
-        float acc[16];
 #pragma unroll
-        for (int x = 0; x < 16; ++x) acc[x] = psi[x];
+        for (int i = 0; i < 16; ++i) {
+            const int e = 4 * (t + kMergeThreads * i), row = e >> 7, col = e & 127;
+            float* d = Phs + row * 129 + col;
+            d[0] = ph[i].x;
+            d[1] = ph[i].y;
+            d[2] = ph[i].z;
+            d[3] = ph[i].w;
+        }
+        const float4 ps = *reinterpret_cast<const float4*>(sc.summ + (size_t)sg * plane + cst +
+                                                          (size_t)r * 128 + c0 + cc);
+        __syncthreads();
+        if (sg + 2 < sc.P) load_phi(sg + 1);  // in flight while this step computes
+        float acc[4] = {ps.x, ps.y, ps.z, ps.w};
+        const float* prow = Phs + r * 129;
+#pragma unroll 8
         for (int d = 0; d < 128; ++d) {
-            const float f = phi[d];
-#pragma unroll
-            for (int x = 0; x < 16; ++x) acc[x] = fmaf(f, X[d][cc + x], acc[x]);
+            const float f = prow[d];
+            const float4 xv = *reinterpret_cast<const float4*>(X + d * kMergeCols + cc);
+            acc[0] = fmaf(f, xv.x, acc[0]);
+            acc[1] = fmaf(f, xv.y, acc[1]);
+            acc[2] = fmaf(f, xv.z, acc[2]);
+            acc[3] = fmaf(f, xv.w, acc[3]);
         }
         __syncthreads();
         float* dst = starts + (size_t)(sg + 1) * plane + cst + (size_t)r * 128 + c0 + cc;
 #pragma unroll
-        for (int x = 0; x < 16; ++x) {
-            X[r][cc + x] = acc[x];
+        for (int x = 0; x < 4; ++x) {
+            X[r * kMergeCols + cc + x] = acc[x];
             dst[x] = acc[x];
         }
         __syncthreads();
     }
 }
+constexpr size_t kMergeSmem = (128 * 129 + 128 * kMergeCols) * sizeof(float);
 
 // Fused schedule for few chains of fixed-length sequences: one persistent CTA per SM.
 // CTAs 0 .. nc - 1 each run the per-chain recurrence of chain b = n H + h; every other
@@ -1650,7 +1677,10 @@ cudaError_t launch_tc(const void* q, const void* k, const void* v, const float* 
         kda_h_o_scan<<<(unsigned)(2 * sc.P * sc.nc), kHoThreads, kHoSmem, s>>>(records, cx, L.max_chunks, sc,
                                                                              s0, ob, sN, H, status);
         if (cudaError_t e = cudaGetLastError()) return e;
-        kda_scan_merge<<<dim3((unsigned)sc.nc, 4), kMergeThreads, 0, s>>>(
+        if (cudaError_t e = cudaFuncSetAttribute(kda_scan_merge, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)kMergeSmem))
+            return e;
+        kda_scan_merge<<<dim3((unsigned)sc.nc, 128 / kMergeCols), kMergeThreads, kMergeSmem, s>>>(
             sc, s0, reinterpret_cast<float*>(ws + L.starts_off));
         if (cudaError_t e = cudaGetLastError()) return e;
         sc.mode = 2;
