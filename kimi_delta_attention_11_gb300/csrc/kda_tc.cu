@@ -38,10 +38,19 @@
 //   warps read the output rows, so that reading them (which waits while the next chunk's
 //   product runs) stays off the chain; one warp issues copies and products.
 // sliced::kda_h_o_sliced_tc: the same recurrence untransposed with operands in shared
-//   memory, one CTA per 64-column value slice: faster when the chains are few.
-//   Every tcgen05 product here is bound by a fixed cost per K=16 step (about 90 cycles
-//   from shared memory, 105 with A in tensor memory, for N <= 128), so the chain keeps
-//   its products to the three the method needs.
+//   memory, one CTA per 64-column value slice: faster when the chains are few and the two
+//   stages run as separate kernels.
+// kda_fused_tc: both stages in one cooperative launch for few fixed-length chains: some
+//   CTAs run the per-chain recurrence (ho_chain) and poll record flags that the other
+//   CTAs' persistent intra lanes (intra_unit, two per CTA) set as they finish records.
+// kda_h_o_scan / kda_scan_merge: chunk-parallel state scan for very few long chains:
+//   segment summaries by the per-chain recurrence, a merge of segment start states, and
+//   the replay of every segment (Tokamax design doc, context-parallel section).
+//   MMAs are issued by a whole converged warp through elect.sync (mma_bf16_w): a tcgen05
+//   product then runs at the pipe's rate (about 48 cycles per M128 x K16 step for N <= 64,
+//   64 for N 128, whatever the operand majorness), and the chained recurrence is bound by
+//   its dependent product groups and hand-offs, so it keeps its products to the three the
+//   method needs.
 #include <mutex>
 
 #include "kda_internal.cuh"
@@ -166,16 +175,18 @@ static_assert(4 * 16 * kBs * 4 <= IntraMap::END - IntraMap::MISC, "X blocks over
 // Rec: the record form (TcRecord for the per-chain recurrence kernel, TcRecordS for the
 // value-sliced one).
 // `sm` is the lane's 1024-aligned shared-memory base, `tmem` its 256 tensor-memory
-// columns.  With `flag`, the record is published once complete: the bulk stores are
-// waited for, then *flag is set with release semantics (the recurrence CTA of the same
-// launch polls it).  Returns false after an expired wait.
+// columns, k the number of chunk-heads the lane ran before (mbarrier phases).  With
+// `prev_flag`, the lane's previous record is published during this one's solve: the
+// thread that stored it waits for its bulk stores, then sets *prev_flag with release
+// semantics (the recurrence CTA of the same launch polls it).  Returns false after an
+// expired wait.
 template <bool kOpts, typename Rec, int kLid>
 __device__ __forceinline__ bool intra_unit(const CUtensorMap* tmq, const CUtensorMap* tmk,
                                            const CUtensorMap* tmv, const CUtensorMap* tmg,
                                            const float* __restrict__ beta, float scale,
                                            const GateArgs& ga, int H, const ChunkIndex& cx,
                                            long long c, int h, uint8_t* __restrict__ rec,
-                                           int* __restrict__ prev_flag, bool publish,
+                                           int* __restrict__ prev_flag,
                                            uint8_t* sm, uint32_t tmem, int lid_arg,
                                            int tid, uint32_t k, int* __restrict__ status) {
     // kLid >= 0: the lane index is a constant (the standalone kernel); -1: lid_arg
@@ -721,7 +732,6 @@ __device__ __forceinline__ bool intra_unit(const CUtensorMap* tmq, const CUtenso
     // A published record's direct stores (query and key rows, gamma) by every thread are
     // ordered before its flag by the lane barriers that follow and the publishing
     // thread's gpu-scope fence before the release store (the fence is cumulative).
-    (void)publish;
 
 teardown:
     tc_fence_before();
@@ -764,7 +774,7 @@ kda_intra_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     tc_fence_after();
     const uint32_t tmem = __shfl_sync(0xffffffffu, tmem_base, 0);
     intra_unit<kOpts, Rec, 0>(&tm_q, &tm_k, &tm_v, &tm_g, beta, scale, ga, H, cx, c, h,
-                              records + ((size_t)slot * H + h) * Rec::bytes, nullptr, false, sm, tmem,
+                              records + ((size_t)slot * H + h) * Rec::bytes, nullptr, sm, tmem,
                               0, threadIdx.x, 0u, status);
     tc_fence_before();
     __syncthreads();
@@ -1230,7 +1240,7 @@ struct FusedArgs {
 };
 
 // One intra lane of the fused kernel: units u0, u0 + lanes, ... (chunk j = u / nc of chain
-// u % nc), each record published when the next one's tiles load (the last at the end).
+// u % nc), each record published during the next one's solve (the last at the end).
 // Both lanes of a CTA run the same code (one copy: the kernel is large, and instruction
 // fetch stalls when the SM alternates between two copies).
 template <bool kOpts>
@@ -1254,7 +1264,7 @@ __device__ __forceinline__ void intra_lane(const FusedArgs& A, uint8_t* sm, uint
         const int h = (int)(u % nc) % H;
         ok = intra_unit<kOpts, TcRecord, -1>(&A.tq, &A.tk, &A.tv, &A.tg, A.beta, A.scale, A.ga, H, A.cx,
                                              c, h, A.records + ((size_t)c * H + h) * TcRecord::bytes,
-                                             prev, true, sm, tmem, lid, tid_u, k, A.status);
+                                             prev, sm, tmem, lid, tid_u, k, A.status);
         if (!ok) break;
     }
     if (ok && k > 0 && tid == kStoreThread) {  // the lane's last record (its storing thread)
