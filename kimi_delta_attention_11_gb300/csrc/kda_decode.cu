@@ -7,9 +7,12 @@
 // The output is folded so that the state is read and written once:
 //   o = scale (S_bar^T q + beta (k . q) e).
 //
-// One CTA of V * K/64 threads per (sequence, head); thread (j, ks) owns rows 64 ks ..
-// 64 ks + 63 of column j of the K x V fp32 state in registers (the warp's loads and stores
-// of one row are contiguous); the two dot products are summed over the key slices in
+// One CTA of 256 threads per (sequence, head) (the kernel can also cut V into slices of
+// kDecCols columns, each column of the state being updated from its own dot products;
+// 64-column slices of 128 threads measured slower, 34.1 against 32.3 us).  Thread (row
+// group rg, column group cg) owns K / RG consecutive key rows of the 4 value columns
+// 4 cg .. 4 cg + 3 in registers, read and written as 16-byte vectors (a warp's accesses
+// to a row are contiguous); the two dot products are summed over the row groups in
 // shared memory.  The step is bound by the state's HBM traffic (2 K V 4 bytes per
 // sequence-head).
 #include <cuda_bf16.h>
@@ -33,15 +36,20 @@ __device__ __forceinline__ float from_f<float>(float x) { return x; }
 template <>
 __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 
+constexpr int kDecThreads = 256;
+constexpr int kDecCols = 128;  // value columns per CTA (all of V when V <= 128)
+
 template <typename T, int K, int V>
-__global__ void __launch_bounds__(V * (K / 64))
+__global__ void __launch_bounds__(kDecThreads)
 kda_decode_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                   const float* __restrict__ g, const float* __restrict__ beta, float scale,
                   GateArgs ga, float* __restrict__ state, T* __restrict__ o, int H) {
-    constexpr int KS = K / 64, NT = V * KS;  // KS key slices of 64 rows per column
-    __shared__ float sq[K], sk[K], sa[K], red[2][NT / 32], part[2][KS][V];
-    const int nh = blockIdx.x, h = nh % H, t = threadIdx.x;
-    const int j = t % V, ks = t / V;  // column j, key rows 64 ks .. 64 ks + 63
+    constexpr int VS = V < kDecCols ? V : kDecCols, SPLIT = V / VS;
+    constexpr int NT = kDecThreads, CG = VS / 4, RG = NT / CG, RPT = K / RG;
+    static_assert(NT % CG == 0 && K % RG == 0 && V % VS == 0, "decode thread layout");
+    __shared__ float sq[K], sk[K], sa[K], red[2][NT / 32], part[2][RG][VS];
+    const int nh = blockIdx.x / SPLIT, c0 = VS * (blockIdx.x % SPLIT), h = nh % H, t = threadIdx.x;
+    const int cg = t % CG, rg = t / CG;  // columns c0 + 4 cg .., rows RPT rg .. RPT rg + RPT - 1
     const size_t vec = (size_t)nh * K;
     // gate (activated in the kernel when asked, Tokamax design doc 9.1.3), decay, and
     // the (optionally L2-normalised) query and key, shared by the CTA
@@ -82,43 +90,69 @@ kda_decode_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __r
         }
         __syncthreads();
     }
-    float* col = state + (size_t)nh * K * V + (size_t)(64 * ks) * V + j;
-    const float* kk = sk + 64 * ks;
-    const float* qq = sq + 64 * ks;
-    const float* aa = sa + 64 * ks;
-    float s[64];
-    float pred = 0.f, read = 0.f;
+    float4* rows = reinterpret_cast<float4*>(state + (size_t)nh * K * V + (size_t)(RPT * rg) * V + c0) + cg;
+    const int d0 = RPT * rg;
+    float4 s[RPT];
 #pragma unroll
-    for (int d = 0; d < 64; ++d) {
-        s[d] = aa[d] * col[(size_t)d * V];
-        pred = fmaf(s[d], kk[d], pred);
-        read = fmaf(s[d], qq[d], read);
+    for (int r = 0; r < RPT; ++r) s[r] = rows[(size_t)r * (V / 4)];  // all loads issued first
+    float pred[4] = {0.f, 0.f, 0.f, 0.f}, rd[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) {
+        const float a = sa[d0 + r], kd = sk[d0 + r], qd = sq[d0 + r];
+        s[r].x *= a;
+        s[r].y *= a;
+        s[r].z *= a;
+        s[r].w *= a;
+        pred[0] = fmaf(s[r].x, kd, pred[0]);
+        pred[1] = fmaf(s[r].y, kd, pred[1]);
+        pred[2] = fmaf(s[r].z, kd, pred[2]);
+        pred[3] = fmaf(s[r].w, kd, pred[3]);
+        rd[0] = fmaf(s[r].x, qd, rd[0]);
+        rd[1] = fmaf(s[r].y, qd, rd[1]);
+        rd[2] = fmaf(s[r].z, qd, rd[2]);
+        rd[3] = fmaf(s[r].w, qd, rd[3]);
     }
-    part[0][ks][j] = pred;
-    part[1][ks][j] = read;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        part[0][rg][4 * cg + c] = pred[c];
+        part[1][rg][4 * cg + c] = rd[c];
+    }
     float kq = 0.f;
 #pragma unroll 8
     for (int d = 0; d < K; ++d) kq = fmaf(sk[d], sq[d], kq);
     __syncthreads();
-    pred = 0.f;
-    read = 0.f;
+    float be[4];
 #pragma unroll
-    for (int x = 0; x < KS; ++x) {
-        pred += part[0][x][j];
-        read += part[1][x][j];
+    for (int c = 0; c < 4; ++c) {
+        float p = 0.f, x = 0.f;
+#pragma unroll
+        for (int w = 0; w < RG; ++w) {
+            p += part[0][w][4 * cg + c];
+            x += part[1][w][4 * cg + c];
+        }
+        pred[c] = p;
+        rd[c] = x;
+        be[c] = beta[nh] * (to_f(v[(size_t)nh * V + c0 + 4 * cg + c]) - p);
     }
-    const float e = to_f(v[(size_t)nh * V + j]) - pred;
-    const float be = beta[nh] * e;
 #pragma unroll
-    for (int d = 0; d < 64; ++d) col[(size_t)d * V] = fmaf(be, kk[d], s[d]);
-    if (ks == 0) o[(size_t)nh * V + j] = from_f<T>(scale * fmaf(be, kq, read));
+    for (int r = 0; r < RPT; ++r) {
+        const float kd = sk[d0 + r];
+        rows[(size_t)r * (V / 4)] = make_float4(fmaf(be[0], kd, s[r].x), fmaf(be[1], kd, s[r].y),
+                                           fmaf(be[2], kd, s[r].z), fmaf(be[3], kd, s[r].w));
+    }
+    if (rg == 0) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            o[(size_t)nh * V + c0 + 4 * cg + c] = from_f<T>(scale * fmaf(be[c], kq, rd[c]));
+    }
 }
 
 template <typename T, int K, int V>
 cudaError_t launch_decode_typed(const void* q, const void* k, const void* v, const float* g,
                                 const float* beta, float scale, const GateArgs& ga, float* state,
                                 void* o, int N, int H, cudaStream_t s) {
-    kda_decode_kernel<T, K, V><<<(unsigned)N * H, V * (K / 64), 0, s>>>(
+    constexpr int split = V < kDecCols ? 1 : V / kDecCols;
+    kda_decode_kernel<T, K, V><<<(unsigned)N * H * split, kDecThreads, 0, s>>>(
         static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v), g, beta,
         scale, ga, state, static_cast<T*>(o), H);
     return cudaGetLastError();
