@@ -111,10 +111,20 @@ def _activated(orc, gd, graw, q, k):
 
 
 @pytest.mark.parametrize("form", list(GATES))
-@pytest.mark.parametrize("path", ["tc_bf16", "tc_bf16_many_chains", "simt_f32"])
-def test_gate_activation_fwd(kda, orc, form, path):
+@pytest.mark.parametrize("path", ["tc_bf16", "tc_bf16_many_chains", "tc_bf16_two", "tc_bf16_scan",
+                                  "simt_f32"])
+def test_gate_activation_fwd(kda, orc, form, path, monkeypatch):
+    """In-kernel gate activation and q/k normalisation on every path and schedule:
+    fused (tc_bf16), per-chain two kernels (many chains), value-sliced two kernels (forced),
+    scan (forced), and the exact CUDA-core path."""
     dtype, K = (torch.float32, 64) if path == "simt_f32" else (torch.bfloat16, 128)
     B, T, H = (2, 150, 3) if path != "tc_bf16_many_chains" else (6, 90, 14)
+    if path == "tc_bf16_two":
+        monkeypatch.setenv("KDA_SCHEDULE", "two")
+    if path == "tc_bf16_scan":
+        B, T, H = 1, 64 * 9 + 11, 2
+        monkeypatch.setenv("KDA_SCHEDULE", "scan")
+        assert kda.schedule(B, T, H, K, K) == "scan"
     g = torch.Generator().manual_seed(5 + len(form) + K)
     q = torch.randn((B, T, H, K), generator=g).to(dtype)   # not normalised: the kernel does it
     k = torch.randn((B, T, H, K), generator=g).to(dtype)
