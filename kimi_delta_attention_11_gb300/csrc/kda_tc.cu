@@ -161,7 +161,7 @@ constexpr size_t kIntraSmem = IntraMap::END + 1024;  // + alignment slack
 // the 16x16 block products hit distinct banks.
 constexpr int kLs = 72, kBs = 20;
 // The thread that issues (and, for published records, completes) the record's bulk stores:
-// lane 0 of the last warp, which is idle in the solve stage where the completion is waited.
+// lane 0 of the last warp.
 constexpr int kStoreThread = kIntraThreads - 32;
 static_assert(IntraMap::LF + 64 * kLs * 4 <= IntraMap::RA + 32768, "L tile overflows");
 static_assert(IntraMap::JB + 6 * 16 * kBs * 4 <= IntraMap::AIA, "J blocks overflow");
@@ -176,16 +176,16 @@ static_assert(4 * 16 * kBs * 4 <= IntraMap::END - IntraMap::MISC, "X blocks over
 // value-sliced one).
 // `sm` is the lane's 1024-aligned shared-memory base, `tmem` its 256 tensor-memory
 // columns, k the number of chunk-heads the lane ran before (mbarrier phases).  With
-// `prev_flag`, the lane's previous record is published during this one's solve: the
-// thread that stored it waits for its bulk stores, then sets *prev_flag with release
-// semantics (the recurrence CTA of the same launch polls it).  Returns false after an
-// expired wait.
+// `prev_flag`, the lane's previous record is published during this one's second relation
+// product: the thread that stored it waits for its bulk stores, then sets *prev_flag with
+// release semantics (the recurrence CTA of the same launch polls it).  Returns false after
+// an expired wait.
 template <bool kOpts, typename Rec, int kLid>
 __device__ __forceinline__ bool intra_unit(const CUtensorMap* tmq, const CUtensorMap* tmk,
                                            const CUtensorMap* tmv, const CUtensorMap* tmg,
                                            const float* __restrict__ beta, float scale,
-                                           const GateArgs& ga, int H, const ChunkIndex& cx,
-                                           long long c, int h, uint8_t* __restrict__ rec,
+                                           const GateArgs& ga, int H, const int4 ent, int h,
+                                           uint8_t* __restrict__ rec,
                                            int* __restrict__ prev_flag,
                                            uint8_t* sm, uint32_t tmem, int lid_arg,
                                            int tid, uint32_t k, int* __restrict__ status) {
@@ -199,7 +199,6 @@ __device__ __forceinline__ bool intra_unit(const CUtensorMap* tmq, const CUtenso
     uint64_t& bar_wu = s_bar_wu[lid];
     const uint32_t lane_bar = 1 + (uint32_t)lid;
     auto lane_sync = [&]() { named_bar_sync(lane_bar, kIntraThreads); };
-    const int4 ent = cx.chunk(c);
     const int t0 = ent.y, len = ent.z;
     const uint32_t sb = smem_u32(sm);
     float* refs = reinterpret_cast<float*>(sm + M::REFS);
@@ -461,6 +460,16 @@ __device__ __forceinline__ bool intra_unit(const CUtensorMap* tmq, const CUtenso
         }
         mma_commit_w(&bar_rel);
     }
+    // The lane's previous record is published while these products run, by the thread that
+    // stored it (lane 0 of the last warp): its bulk stores, issued some microseconds ago,
+    // are waited for, then the flag is set with release semantics.  The other threads'
+    // direct stores to that record precede the lane barriers passed since.
+    if (prev_flag && tid == kStoreThread) {
+        bulk_wait_all();
+        fence_proxy_async_global();
+        __threadfence();
+        st_release_gpu(prev_flag, 1);
+    }
     mbar_wait_abortable(&bar_rel, 1, status, abort_flag);
     tc_fence_after();
     lane_sync();
@@ -587,15 +596,6 @@ __device__ __forceinline__ bool intra_unit(const CUtensorMap* tmq, const CUtenso
         lane_sync();
         // Stage 3 (warps 0-2): X20 = J21 J10 - J20, X31 = J32 J21 - J31,
         // X30 = J31 J10 + J32 J20 - J30 - J32 (J21 J10) (warp 2, through a scratch block).
-        // The previous record of this lane is published by the thread that stored it
-        // (warp 7, idle in this stage): its bulk stores, long complete, are waited for,
-        // then the flag is set with release semantics.
-        if (prev_flag && tid == kStoreThread) {
-            bulk_wait_all();
-            fence_proxy_async_global();
-            __threadfence();
-            st_release_gpu(prev_flag, 1);
-        }
         if (warp < 3) {
             float acc[2][4];
             const float* J = JB;
@@ -726,7 +726,7 @@ __device__ __forceinline__ bool intra_unit(const CUtensorMap* tmq, const CUtenso
         }
         bulk_commit();
         // only the shared-memory sources must outlive the copies here; a record that is
-        // published is waited for during the next one's solve (or after the last)
+        // published is waited for during the next one's relation products (or after the last)
         bulk_wait_read_all();
     }
     // A published record's direct stores (query and key rows, gamma) by every thread are
@@ -773,7 +773,7 @@ kda_intra_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ C
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = __shfl_sync(0xffffffffu, tmem_base, 0);
-    intra_unit<kOpts, Rec, 0>(&tm_q, &tm_k, &tm_v, &tm_g, beta, scale, ga, H, cx, c, h,
+    intra_unit<kOpts, Rec, 0>(&tm_q, &tm_k, &tm_v, &tm_g, beta, scale, ga, H, cx.chunk(c), h,
                               records + ((size_t)slot * H + h) * Rec::bytes, nullptr, sm, tmem,
                               0, threadIdx.x, 0u, status);
     tc_fence_before();
@@ -1240,39 +1240,51 @@ struct FusedArgs {
 };
 
 // One intra lane of the fused kernel: units u0, u0 + lanes, ... (chunk j = u / nc of chain
-// u % nc), each record published during the next one's solve (the last at the end).
+// u % nc), each record published during the next one's relation products (the last at
+// the end).
 // Both lanes of a CTA run the same code (one copy: the kernel is large, and instruction
 // fetch stalls when the SM alternates between two copies).
 template <bool kOpts>
 __device__ __forceinline__ void intra_lane(const FusedArgs& A, uint8_t* sm, uint32_t tmem, int lid, int tid) {
-    const int nc = A.nc, H = A.H;
-    const long long u0 = 2ll * ((long long)blockIdx.x - nc) + lid;
+    const int nc = A.nc, H = A.H, T = A.cx.T;
     const long long lanes = 2ll * ((long long)gridDim.x - nc);
     const long long units = (long long)nc * A.cx.nct;
-    auto chunk_of = [&](long long u) { return (long long)((int)(u % nc) / H) * A.cx.nct + (int)(u / nc); };
+    long long u = 2ll * ((long long)blockIdx.x - nc) + lid;
+    // unit u is chunk j = u / nc of chain n = u % nc; from one unit of the lane to the next
+    // (j, n) advance by (lanes / nc, lanes % nc) with a carry, so that no unit pays for
+    // 64-bit divisions (a chain of them measured ~2 us between chunk-heads)
+    const int dj = (int)(lanes / nc), dn = (int)(lanes % nc);
+    int j = (int)(u / nc), n = (int)(u % nc);
+    int* prev = nullptr;
     uint32_t k = 0;
     bool ok = true;
 #pragma unroll 1
-    for (long long u = u0; u < units; u += lanes, ++k) {
+    for (; u < units; u += lanes, ++k) {
         // the thread index goes through an empty asm each unit, so that the compiler
         // derives the per-thread offsets inside the unit instead of holding them across
         // the loop (registers are the intra lane's limit)
         int tid_u = tid;
         asm volatile("" : "+r"(tid_u));
-        int* prev = k > 0 ? A.flags + (size_t)chunk_of(u - lanes) * H + (int)((u - lanes) % nc) % H : nullptr;
-        const long long c = chunk_of(u);
-        const int h = (int)(u % nc) % H;
-        ok = intra_unit<kOpts, TcRecord, -1>(&A.tq, &A.tk, &A.tv, &A.tg, A.beta, A.scale, A.ga, H, A.cx,
-                                             c, h, A.records + ((size_t)c * H + h) * TcRecord::bytes,
+        const int b = n / H, h = n - b * H;  // sequence, head
+        const long long c = (long long)b * A.cx.nct + j;
+        const int4 ent = make_int4(b, b * T + j * kChunk, min(kChunk, T - j * kChunk), j);
+        ok = intra_unit<kOpts, TcRecord, -1>(&A.tq, &A.tk, &A.tv, &A.tg, A.beta, A.scale, A.ga, H, ent,
+                                             h, A.records + ((size_t)c * H + h) * TcRecord::bytes,
                                              prev, sm, tmem, lid, tid_u, k, A.status);
         if (!ok) break;
+        prev = A.flags + (size_t)c * H + h;
+        j += dj;
+        n += dn;
+        if (n >= nc) {
+            n -= nc;
+            ++j;
+        }
     }
     if (ok && k > 0 && tid == kStoreThread) {  // the lane's last record (its storing thread)
-        const long long ul = u0 + (long long)(k - 1) * lanes;
         bulk_wait_all();
         fence_proxy_async_global();
         __threadfence();
-        st_release_gpu(A.flags + (size_t)chunk_of(ul) * H + (int)(ul % nc) % H, 1);
+        st_release_gpu(prev, 1);
     }
 }
 
