@@ -1251,8 +1251,8 @@ __device__ __forceinline__ void intra_lane(const FusedArgs& A, uint8_t* sm, uint
     const long long units = (long long)nc * A.cx.nct;
     long long u = 2ll * ((long long)blockIdx.x - nc) + lid;
     // unit u is chunk j = u / nc of chain n = u % nc; from one unit of the lane to the next
-    // (j, n) advance by (lanes / nc, lanes % nc) with a carry, so that no unit pays for
-    // 64-bit divisions (a chain of them measured ~2 us between chunk-heads)
+    // (j, n) advance by (lanes / nc, lanes % nc) with a carry: 64-bit divisions here took
+    // ~0.7 us of the 2.2 us that passed between two chunk-heads of a lane
     const int dj = (int)(lanes / nc), dn = (int)(lanes % nc);
     int j = (int)(u / nc), n = (int)(u % nc);
     int* prev = nullptr;
