@@ -100,6 +100,18 @@ def status_string(status: int) -> str:
         return STATUS_NAMES.get(status, "unknown")
 
 
+def _check(name: str, t: torch.Tensor, shape: tuple, device: torch.device) -> None:
+    """The library reads and writes through raw pointers with the sizes it is given, so
+    every tensor must have the shape those sizes imply, be contiguous and live on the
+    calling device."""
+    if not t.is_cuda or t.device != device:
+        raise ValueError(f"{name} must be a CUDA tensor on {device}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
 def _ptr(t: Optional[torch.Tensor]):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
@@ -178,32 +190,48 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
     in [-5, 0) (sigmoid form), qk_l2norm=bool); g then holds raw gates when a_log is set.
     """
     lib = load_library()
+    if q.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, g must be [B,T,H,K] and v [B,T,H,V]")
     B, T, H, K = q.shape
     V = v.shape[-1]
     if scale is None:
         scale = K ** -0.5
-    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta)):
-        if not t.is_cuda or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    dev = q.device
     if k.dtype != q.dtype or v.dtype != q.dtype or q.dtype not in DTYPE_CODES:
         raise ValueError("q, k, v must share one dtype, bf16 or fp32")
     if g.dtype != torch.float32 or beta.dtype != torch.float32:
         raise ValueError("g and beta must be fp32")
-    if initial_state is not None and (initial_state.dtype != torch.float32
-                                      or not initial_state.is_contiguous()):
-        raise ValueError("initial_state must be contiguous fp32")
+    _check("q", q, (B, T, H, K), dev)
+    _check("k", k, (B, T, H, K), dev)
+    _check("v", v, (B, T, H, V), dev)
+    _check("g", g, (B, T, H, K), dev)
+    _check("beta", beta, (B, T, H), dev)
     num_seqs = 0
     if cu_seqlens is not None:
-        if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda:
-            raise ValueError("cu_seqlens must be an int32 CUDA tensor")
+        if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1:
+            raise ValueError("cu_seqlens must be a 1-D int32 CUDA tensor")
+        _check("cu_seqlens", cu_seqlens, tuple(cu_seqlens.shape), dev)
         num_seqs = cu_seqlens.numel() - 1
     N = num_seqs if cu_seqlens is not None else B
-    dev = q.device
+    if initial_state is not None:
+        if initial_state.dtype != torch.float32:
+            raise ValueError("initial_state must be fp32")
+        _check("initial_state", initial_state, (N, H, K, V), dev)
     need = workspace_bytes(B, T, H, K, V, num_seqs, q.dtype, chunk_size)
     if workspace is None or workspace.numel() * workspace.element_size() < need:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    else:
+        _check("workspace", workspace, tuple(workspace.shape), dev)
+    if out is not None:
+        if out.dtype != q.dtype:
+            raise ValueError("out must have q's dtype")
+        _check("out", out, (B, T, H, V), dev)
     o = out if out is not None else torch.empty((B, T, H, V), dtype=q.dtype, device=dev)
     fin = final_state
+    if fin is not None:
+        if fin.dtype != torch.float32:
+            raise ValueError("final_state must be fp32")
+        _check("final_state", fin, (N, H, K, V), dev)
     if fin is None and output_final_state:
         fin = torch.empty((N, H, K, V), dtype=torch.float32, device=dev)
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), chunk_size,
@@ -234,20 +262,26 @@ def decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
     g [N,H,K] fp32, beta [N,H] fp32, state [N,H,K,V] fp32 updated in place.  Returns o
     [N,H,V] in q.dtype.  ``gate`` as for fwd."""
     lib = load_library()
+    if q.dim() != 3 or v.dim() != 3:
+        raise ValueError("q, k, g must be [N,H,K] and v [N,H,V]")
     N, H, K = q.shape
     V = v.shape[-1]
     if scale is None:
         scale = K ** -0.5
-    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("state", state)):
-        if not t.is_cuda or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    dev = q.device
     if k.dtype != q.dtype or v.dtype != q.dtype or q.dtype not in DTYPE_CODES:
         raise ValueError("q, k, v must share one dtype, bf16 or fp32")
     if g.dtype != torch.float32 or beta.dtype != torch.float32 or state.dtype != torch.float32:
         raise ValueError("g, beta and state must be fp32")
-    if tuple(state.shape) != (N, H, K, V):
-        raise ValueError("state must be [N, H, K, V]")
-    o = out if out is not None else torch.empty((N, H, V), dtype=q.dtype, device=q.device)
+    for name, t, shape in (("q", q, (N, H, K)), ("k", k, (N, H, K)), ("v", v, (N, H, V)),
+                           ("g", g, (N, H, K)), ("beta", beta, (N, H)),
+                           ("state", state, (N, H, K, V))):
+        _check(name, t, shape, dev)
+    if out is not None:
+        if out.dtype != q.dtype:
+            raise ValueError("out must have q's dtype")
+        _check("out", out, (N, H, V), dev)
+    o = out if out is not None else torch.empty((N, H, V), dtype=q.dtype, device=dev)
     opts = _gate_struct(gate, H, K)
     st = lib.kda_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
                         _ptr(state), _ptr(o), N, H, K, V, DTYPE_CODES[q.dtype],

@@ -106,6 +106,37 @@ def test_empty_input_returns_initial_state(kda):
     assert o.shape == (1, 0, H, V) and torch.equal(fin, s0)
 
 
+def test_binding_rejects_mismatched_tensors(kda):
+    # the library trusts the sizes it is given, so the binding checks every tensor's shape,
+    # contiguity and device against them before anything is enqueued
+    inp = _base_bf16(T=96, H=2)
+    q, k, v, g, beta = (inp[x] for x in ("q", "k", "v", "g", "beta"))
+    bad = {
+        "k": dict(k=k[:, :64].contiguous()),
+        "v": dict(v=v[:, :64].contiguous()),
+        "g": dict(g=g[:, :, :1].contiguous()),
+        "beta": dict(beta=beta[:, :64].contiguous()),
+        "q non-contiguous": dict(q=q.transpose(1, 2).contiguous().transpose(1, 2)),
+        "initial_state": dict(initial_state=torch.zeros((2, 2, 128, 128), device="cuda")),
+        "out": dict(out=torch.empty((1, 96, 2, 64), dtype=q.dtype, device="cuda")),
+        "final_state": dict(final_state=torch.empty((1, 2, 128, 64), device="cuda")),
+        "cu_seqlens on the host": dict(cu_seqlens=torch.tensor([0, 96], dtype=torch.int32)),
+    }
+    for what, change in bad.items():
+        args = dict(q=q, k=k, v=v, g=g, beta=beta)
+        args.update(change)
+        with pytest.raises(ValueError):
+            kda.fwd(args.pop("q"), args.pop("k"), args.pop("v"), args.pop("g"), args.pop("beta"),
+                    **args)
+    N, H, K, V = 2, 2, 128, 128
+    st = torch.zeros((N, H, K, V), device="cuda")
+    dq = torch.zeros((N, H, K), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ValueError):
+        kda.decode(dq, dq, torch.zeros((N, H, V), dtype=torch.bfloat16, device="cuda"),
+                   torch.zeros((N, H, K), device="cuda"), torch.zeros((N, 1), device="cuda"), st)
+    torch.cuda.synchronize()
+
+
 def _base_bf16(T=200, H=2, seed=41):
     return make_inputs(custom(B=1, T=T, H=H, K=128, V=128, dtype=torch.bfloat16, init_std=0.1,
                               seed=seed), device="cuda")
