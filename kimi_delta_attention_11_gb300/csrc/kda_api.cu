@@ -3,6 +3,7 @@
 // Host-side validation happens before anything is enqueued; then the chunk index, the
 // intra-chunk stage and the state/output recurrence are launched on the caller's
 // stream with no host synchronisation and no allocation.
+#include <atomic>
 #include <limits.h>
 #include <cstdlib>
 #include <cstring>
@@ -131,13 +132,16 @@ kda_status check_sizes(int B, int T, int H, int K, int V, int num_seqs, bool pac
 
 // The library is built for sm_103a only; refuse any other current device up front.
 kda_status check_device() {
-    static int verdict[64];  // 0 unknown, 1 ok, 2 unusable
+    // 0 unknown, 1 ok, 2 unusable; host threads may race to fill an entry, and all of
+    // them write the same value
+    static std::atomic<int> verdict[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
         cudaGetLastError();
         return KDA_ERR_DEVICE;
     }
-    if (verdict[dev] == 0) {
+    int v = verdict[dev].load(std::memory_order_relaxed);
+    if (v == 0) {
         int major = 0, minor = 0;
         const bool ok = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) ==
                             cudaSuccess &&
@@ -145,9 +149,10 @@ kda_status check_device() {
                             cudaSuccess &&
                         major == 10 && minor == 3;
         cudaGetLastError();
-        verdict[dev] = ok ? 1 : 2;
+        v = ok ? 1 : 2;
+        verdict[dev].store(v, std::memory_order_relaxed);
     }
-    return verdict[dev] == 1 ? KDA_OK : KDA_ERR_DEVICE;
+    return v == 1 ? KDA_OK : KDA_ERR_DEVICE;
 }
 
 }  // namespace
