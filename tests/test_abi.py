@@ -144,6 +144,18 @@ def test_binding_fails_loudly_without_library(tmp_path):
         _native.load_library(str(tmp_path / "missing.so"))
 
 
+def test_binding_refuses_host_tensors(lib):
+    # there is no CPU path: host tensors are rejected before the library is called
+    B, T, H, K, V = 1, 64, 2, 64, 64
+    q = torch.zeros((B, T, H, K))
+    with pytest.raises(ValueError, match="CUDA"):
+        kda.fwd(q, q, torch.zeros((B, T, H, V)), q, torch.zeros((B, T, H)))
+    s = torch.zeros((2, H, K, V))
+    d = torch.zeros((2, H, K))
+    with pytest.raises(ValueError, match="CUDA"):
+        kda.decode(d, d, torch.zeros((2, H, V)), d, torch.zeros((2, H)), s)
+
+
 def call_decode(lib, opts=None, **kw):
     a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, scale=0.1, state=FAKE, o=FAKE, N=2, H=1,
              K=64, V=64, dt=1, stream=None)
