@@ -14,14 +14,15 @@
 //       blocks stacked to M = 128) and the block's 16 scaled query rows and 16
 //       beta-scaled key rows the N side (N = 64 for two blocks); two rounds share one
 //       operand buffer.
-//   a4  (I + L)^{-1} in fp32 on CUDA cores from 16 x 16 blocks: D = inverses of the
-//       diagonal blocks, J = D F (F the blocks below the diagonal), X = (I + J)^{-1} by
-//       block forward substitution, (I + L)^{-1} = X D; each block product is computed a
-//       column per thread with the left factor's rows read as broadcast 16-byte loads.
-//       [W | U] = (I + L)^{-1} [D_beta K+ | D_beta V] by one M 128 x N 256 x K 64 MMA
-//       whose B operand is the k and v tiles rescaled in place (token-major, read as an
-//       MN-major operand) (Tokamax design doc Eq. (6)-(7)).  K_bar = k 2^{G_C - G} and
-//       the gated, scaled query Qg (9.1.5).
+//   a4  (I + L)^{-1} from 16 x 16 blocks: D = inverses of the diagonal blocks (fp32
+//       forward substitution on CUDA cores), J = D F (F the blocks below the diagonal),
+//       X = (I + J)^{-1} by block forward substitution, (I + L)^{-1} = X D; the block
+//       products on the warp-level TF32 instruction (tcgen05 needs M >= 64).
+//       W = (I + L)^{-1} D_beta K+ and U = (I + L)^{-1} D_beta V (Tokamax design doc
+//       Eq. (6)-(7)) with the k and v tiles rescaled in place as operands (token-major,
+//       read MN-major): one M 128 x N 256 x K 64 MMA for the value-sliced record; for the
+//       per-chain record W (N 128) and U^T = (D_beta V)^T ((I + L)^{-1})^T (N 64).
+//       K_bar = k 2^{G_C - G} and the gated, scaled query Qg (9.1.5).
 //   The results form one record per (chunk, head) (TcRecord), written as tensor-core
 //   operand images.
 //
