@@ -35,6 +35,7 @@ from workloads import DECODE_WORKLOADS, WORKLOADS, make_decode_inputs, make_inpu
 
 METRIC = "KDA fwd tokens/s and TFLOP/s (bf16, H=16, K=V=128, T=4096); % of roofline"
 UNIT = "tokens/s"
+DECODE_METRIC = "KDA decode step tokens/s (one token per sequence)"
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -220,6 +221,57 @@ def oracle_sample_rate(inp, seconds: float):
     return tokens / dt, orc.threads_used, desc, dt
 
 
+def oracle_decode_rate(spec: dict, seconds: float):
+    """Time the fp64 oracle on whole decode steps of the decode workload (every
+    sequence and head advanced by its one token from its state), repeated for about
+    `seconds`.  Returns (tokens/s, threads, description, seconds per step)."""
+    import oracle
+    orc = oracle.default_oracle()
+    d = make_decode_inputs(**spec)
+    tok = {x: d[x].unsqueeze(1).contiguous() for x in ("q", "k", "v", "g", "beta")}
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        orc.recurrent(tok["q"], tok["k"], tok["v"], tok["g"], tok["beta"], d["scale"],
+                      initial_state=d["state"])
+        reps += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = (time.perf_counter() - t0) / reps
+    desc = (f"fp64 token recurrence, {reps} whole decode steps of {d['N']} sequences x "
+            f"{d['H']} heads; tokens/s = {d['N']}/time per step")
+    return d["N"] / dt, orc.threads_used, desc, dt
+
+
+def run_reference_decode(args, rank, world):
+    if rank != 0:
+        return 0
+    spec = DECODE_WORKLOADS[args.workload]
+    per_step = min(5.0, max(0.2, 60.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_decode_rate(spec, per_step)
+    rates, threads, desc = [], 1, ""
+    for _ in range(args.steps):
+        r, threads, desc, _ = oracle_decode_rate(spec, per_step)
+        rates.append(r)
+    value = statistics.median(rates)
+    line = {
+        "metric": DECODE_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * spec["N"] / value,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference", "config": decode_config(args.workload, spec),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def decode_config(name: str, spec: dict) -> dict:
+    return {"workload": f"{name}: N={spec['N']} H={spec['H']} K={spec['K']} V={spec['V']}",
+            "l2": "flushed between timed steps (write of 4x L2)"}
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return 0
@@ -237,7 +289,7 @@ def run_reference(args, rank, world):
     value = statistics.median(rates)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": 1e3 * w.B * w.T / value if w.T else None,
+        "warmup": args.warmup, "ms_per_step": 1e3 * inp["B"] * inp["T"] / value,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "impl": "reference",
         "config": workload_config(w, inp),
@@ -476,12 +528,11 @@ def run_decode(args, rank, world, local):
     peak, peak_kind = measured_peaks()
     achieved = step_bytes / (ms * 1e-3) / 1e9
     line = {
-        "metric": "KDA decode step tokens/s (one token per sequence)", "value": N * world / (ms * 1e-3),
+        "metric": DECODE_METRIC, "value": N * world / (ms * 1e-3),
         "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if dt == torch.bfloat16 else "f32", "data": "synthetic",
-        "config": {"workload": f"{args.workload}: N={N} H={H} K={K} V={V}",
-                   "l2": "flushed between timed steps (write of 4x L2)"},
+        "config": decode_config(args.workload, spec),
         "roofline": {"bound": "hbm", "kernel": "kda_decode_kernel", "achieved": achieved,
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": f"{peak_kind} hbm_gbs",
@@ -489,6 +540,10 @@ def run_decode(args, rank, world, local):
                      "bytes_per_step": step_bytes},
         "gpu_launches": args.steps, "clocks": clocks, "wall_s_timed": wall,
     }
+    if world == 1 and not args.no_cpu_baseline:
+        r, threads, desc, _ = oracle_decode_rate(spec, min(args.cpu_seconds, 5.0))
+        line["cpu_baseline"] = {"value": r, "unit": "tokens/s", "cores": threads,
+                                "kind": "oracle", "sample": desc}
     print(json.dumps(line), flush=True)
     return 0
 
@@ -509,7 +564,7 @@ def main():
     rank, world, local = dist_info()
     if args.workload in DECODE_WORKLOADS:
         if args.impl == "reference":
-            ap.error("the decode workload has no reference arm")
+            return run_reference_decode(args, rank, world)
         init_dist(world)
         try:
             return run_decode(args, rank, world, local)

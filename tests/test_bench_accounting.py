@@ -53,3 +53,10 @@ def test_short_chunks_and_packed_sequences():
     per = lambda L: (L // 64) * bench.flops_per_chunk(64, 64, 64) + (bench.flops_per_chunk(L % 64, 64, 64) if L % 64 else 0)
     assert a["flops"] == 2 * (per(70) + per(0) + per(130))
     assert a["state_out"] == 3 * 2 * 64 * 64 * 4
+
+
+def test_decode_reference_rate_runs_the_oracle():
+    spec = dict(N=2, H=2, K=64, V=64, dtype=torch.float32, init_std=0.1, seed=3)
+    rate, threads, desc, dt = bench.oracle_decode_rate(spec, 0.0)
+    assert rate > 0 and dt > 0 and threads >= 1
+    assert "2 sequences x 2 heads" in desc
