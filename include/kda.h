@@ -275,6 +275,14 @@ typedef enum {
 int kda_fwd_schedule(int B, int T, int H, int K, int V, int num_seqs, int chunk_size,
                      kda_dtype dtype);
 
+/* The same choice for a device with `sm_count` SMs (152 on a GB300), whichever device is
+ * current, e.g. to plan shapes ahead of a call; the environment override KDA_SCHEDULE
+ * applies as in kda_fwd.  -1 for sizes kda_fwd rejects or a negative sm_count.  With
+ * sm_count 0 neither the fused nor the scan schedule is chosen (both size their grids by
+ * the SM count). */
+int kda_fwd_schedule_for(int B, int T, int H, int K, int V, int num_seqs, int chunk_size,
+                         kda_dtype dtype, int sm_count);
+
 /* Version of this ABI (major * 100 + minor). */
 int kda_abi_version(void);
 

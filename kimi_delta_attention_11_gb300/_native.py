@@ -66,6 +66,7 @@ _SIGNATURES = {
     "kda_abi_version": (_i, []),
     "kda_fwd_launch_count": (_i, [_i, _i, _i, _i, _i, _i, _i, _i]),
     "kda_fwd_schedule": (_i, [_i, _i, _i, _i, _i, _i, _i, _i]),
+    "kda_fwd_schedule_for": (_i, [_i, _i, _i, _i, _i, _i, _i, _i, _i]),
 }
 
 
@@ -143,9 +144,16 @@ SCHEDULES = {0: "two_kernels", 1: "pipelined", 2: "fused", 3: "scan"}
 
 
 def schedule(B: int, T: int, H: int, K: int, V: int, num_seqs: int = 0,
-             dtype: torch.dtype = torch.bfloat16, chunk_size: int = 64) -> str:
-    """Schedule one kda_fwd takes for these sizes on the current device."""
-    n = load_library().kda_fwd_schedule(B, T, H, K, V, num_seqs, chunk_size, DTYPE_CODES[dtype])
+             dtype: torch.dtype = torch.bfloat16, chunk_size: int = 64,
+             sm_count: Optional[int] = None) -> str:
+    """Schedule one kda_fwd takes for these sizes on the current device, or on a device
+    with `sm_count` SMs."""
+    lib = load_library()
+    if sm_count is None:
+        n = lib.kda_fwd_schedule(B, T, H, K, V, num_seqs, chunk_size, DTYPE_CODES[dtype])
+    else:
+        n = lib.kda_fwd_schedule_for(B, T, H, K, V, num_seqs, chunk_size, DTYPE_CODES[dtype],
+                                     int(sm_count))
     if n < 0:
         raise KdaError(1, "kda_fwd_schedule")
     return SCHEDULES[int(n)]

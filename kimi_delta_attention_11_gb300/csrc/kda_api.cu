@@ -39,7 +39,8 @@ int current_sm_count() {
     return sms;
 }
 
-Layout make_layout(int B, int T, int H, int K, int V, int num_seqs, bool packed, kda_dtype dt) {
+Layout make_layout(int B, int T, int H, int K, int V, int num_seqs, bool packed, kda_dtype dt,
+                   int sm_count) {
     Layout L;
     const long long nct = ((long long)T + kChunk - 1) / kChunk;
     L.N = packed ? num_seqs : B;
@@ -56,7 +57,7 @@ Layout make_layout(int B, int T, int H, int K, int V, int num_seqs, bool packed,
     L.fixed = use_tc_path(K, V, dt) && !packed;
     const Schedule want = schedule_request();
     const long long chains = (long long)B * H;
-    const int sms = L.fixed && L.max_chunks > 0 ? current_sm_count() : 0;
+    const int sms = !(L.fixed && L.max_chunks > 0) ? 0 : sm_count >= 0 ? sm_count : current_sm_count();
     // Fused: the recurrences of few chains occupy few SMs for the whole call, so the
     // records are produced on the other SMs while they run (one CTA per SM, both
     // stages in one cooperative launch).  Automatic up to a third of the SMs.
@@ -159,17 +160,23 @@ kda_status check_device() {
 
 extern "C" {
 
-int kda_abi_version(void) { return 102; }
+int kda_abi_version(void) { return 103; }
 
-int kda_fwd_schedule(int B, int T, int H, int K, int V, int num_seqs, int chunk_size,
-                     kda_dtype dtype) {
+int kda_fwd_schedule_for(int B, int T, int H, int K, int V, int num_seqs, int chunk_size,
+                         kda_dtype dtype, int sm_count) {
     const bool packed = num_seqs > 0;
+    if (sm_count < 0) return -1;
     if (check_sizes(B, T, H, K, V, num_seqs, packed, chunk_size, dtype) != KDA_OK) return -1;
-    const Layout L = make_layout(B, T, H, K, V, num_seqs, packed, dtype);
+    const Layout L = make_layout(B, T, H, K, V, num_seqs, packed, dtype, sm_count);
     if (L.fused) return KDA_SCHEDULE_FUSED;
     if (L.scan) return KDA_SCHEDULE_SCAN;
     if (L.span > 0) return KDA_SCHEDULE_PIPELINED;
     return KDA_SCHEDULE_TWO_KERNELS;
+}
+
+int kda_fwd_schedule(int B, int T, int H, int K, int V, int num_seqs, int chunk_size,
+                     kda_dtype dtype) {
+    return kda_fwd_schedule_for(B, T, H, K, V, num_seqs, chunk_size, dtype, current_sm_count());
 }
 
 int kda_fwd_launch_count(int B, int T, int H, int K, int V, int num_seqs, int chunk_size,

@@ -190,7 +190,9 @@ inline bool use_tc_path(int K, int V, kda_dtype dt) {
 bool make_tmap_2d(CUtensorMap* map, const void* base, bool bf16, uint64_t inner, uint64_t outer,
                   uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, bool swizzle128);
 
-Layout make_layout(int B, int T, int H, int K, int V, int num_seqs, bool packed, kda_dtype dt);
+// sm_count < 0: the current device's SM count (0 when no device is current)
+Layout make_layout(int B, int T, int H, int K, int V, int num_seqs, bool packed, kda_dtype dt,
+                   int sm_count = -1);
 
 // Launchers (return cudaGetLastError() of their launches).
 cudaError_t launch_chunk_index(const int32_t* cu_seqlens, int N, int T, const Layout& L,

@@ -38,7 +38,7 @@ def test_status_strings(lib):
     for s in range(8):
         assert lib.kda_status_string(s).decode()
     assert lib.kda_status_string(99).decode() == "unknown status"
-    assert lib.kda_abi_version() == 102
+    assert lib.kda_abi_version() == 103
 
 
 def test_launch_count(lib):
@@ -69,6 +69,43 @@ def test_schedule_query(lib):
     assert sc(1, 37000, 32, 128, 128, 8, 64, bf16) == 0             # packed
     assert sc(1, 131072, 32, 128, 128, 0, 64, f32) == 0             # fp32 path
     assert sc(2, 4096, 16, 128, 128, 0, 32, bf16) == -1             # rejected sizes
+
+
+@pytest.mark.parametrize("sizes,sms,expected", [
+    ((2, 4096, 16, 0), 152, "fused"),          # dense: 32 chains, a fifth of the SMs
+    ((1, 131072, 32, 0), 152, "fused"),        # long: 32 chains of 2048 chunks
+    ((1, 262144, 2, 0), 152, "scan"),          # two chains of 4096 chunks
+    ((1, 64 * 100, 2, 0), 152, "fused"),       # few chains, too short to scan
+    ((32, 2048, 32, 0), 152, "two_kernels"),   # serving: 1024 chains
+    ((1, 37000, 32, 8), 152, "two_kernels"),   # packed sequences
+    ((1, 131072, 32, 0), 0, "pipelined"),      # no SM count: neither fused nor scanned
+    ((2, 4096, 16, 0), 64, "two_kernels"),     # 32 chains need three times as many SMs
+    ((2, 4096, 16, 0), 96, "fused"),
+    ((1, 262144, 2, 0), 15, "fused"),          # the scan wants eight SMs per chain
+    ((1, 262144, 2, 0), 16, "scan"),
+])
+def test_schedule_rules_for_a_given_sm_count(sizes, sms, expected, monkeypatch):
+    """The host's choice of schedule (kda_fwd_schedule_for), which kda_fwd makes with the
+    current device's SM count."""
+    monkeypatch.delenv("KDA_SCHEDULE", raising=False)
+    B, T, H, nseq = sizes
+    assert kda.schedule(B, T, H, 128, 128, nseq, sm_count=sms) == expected
+
+
+def test_schedule_override_and_rejections(lib, monkeypatch):
+    sc = lambda *a: lib.kda_fwd_schedule_for(*a)
+    bf16, f32 = 0, 1
+    monkeypatch.setenv("KDA_SCHEDULE", "two")
+    assert sc(2, 4096, 16, 128, 128, 0, 64, bf16, 152) == 0
+    monkeypatch.setenv("KDA_SCHEDULE", "fused")             # forced where it can run
+    assert sc(2, 4096, 16, 128, 128, 0, 64, bf16, 64) == 2
+    assert sc(2, 4096, 16, 128, 128, 0, 64, bf16, 63) == 0  # 32 chains need 64 SMs
+    monkeypatch.setenv("KDA_SCHEDULE", "scan")
+    assert sc(2, 4096, 16, 128, 128, 0, 64, bf16, 152) == 3
+    monkeypatch.delenv("KDA_SCHEDULE")
+    assert sc(1, 131072, 32, 128, 128, 0, 64, f32, 152) == 0  # fp32 path
+    assert sc(2, 4096, 16, 128, 128, 0, 32, bf16, 152) == -1  # rejected sizes
+    assert sc(2, 4096, 16, 128, 128, 0, 64, bf16, -1) == -1   # negative SM count
 
 
 def test_workspace_bytes_rules(lib):
