@@ -140,6 +140,7 @@ size_t kda_fwd_workspace_bytes(int B, int T, int H, int K, int V, int num_seqs,
  *   scan       at most an eighth of the SMs' count of chains and at least 128 chunks per
  *              sequence: chunk-parallel state scan (segment summaries, a per-chain merge of
  *              segment start states, then every segment replayed): four launches.
+ *              Where both the scan and the fused rule hold, the scan is taken.
  * The environment variable KDA_SCHEDULE ("two", "pipelined", "fused", "scan") forces a schedule
  * where the sizes allow it (read at workspace sizing and at each call, which must agree).
  * kda_fwd_launch_count gives the number of kernel launches. */
