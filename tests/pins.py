@@ -144,6 +144,32 @@ def pin_linear_attention(oracle, forms=FORMS):
 
 
 # ---------------------------------------------------------------------------
+# Delta-rule retrieval: a full-strength write is read back exactly
+# ---------------------------------------------------------------------------
+
+def pin_delta_rule_retrieval(oracle, forms=FORMS):
+    """With beta_t = 1 and a unit key, the write replaces what the decayed state held at
+    k_t: S_t^T k_t = (Diag(alpha_t) S_{t-1})^T (I - k_t k_t^T) k_t + v_t (k_t . k_t) = v_t,
+    whatever S_0 and the decays are (Tokamax 9.1.2, the delta-correction form of Eq. (1):
+    the correction v_t - S^T k_t is written back in full).  So querying with q_t = k_t
+    gives o_t = scale * v_t at every token."""
+    rng = np.random.default_rng(21)
+    B, T, H, K, V = 2, 40, 2, 16, 8
+    k = rng.standard_normal((B, T, H, K))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((B, T, H, V))
+    g = -5.0 * rng.random((B, T, H, K))
+    beta = np.ones((B, T, H))
+    s0 = rng.standard_normal((B, H, K, V))
+    scale = 0.61
+    for form in forms:
+        o, fin = run(oracle, form, k.copy(), k, v, g, beta, scale, initial_state=s0)
+        assert np.allclose(o, scale * v, rtol=0, atol=1e-10), f"retrieval mismatch ({form})"
+        last = np.einsum("bhkv,bhk->bhv", fin, k[:, -1])
+        assert np.allclose(last, v[:, -1], rtol=0, atol=1e-10), f"final-state retrieval ({form})"
+
+
+# ---------------------------------------------------------------------------
 # P-2: beta = 0 freezes the state up to its decay
 # ---------------------------------------------------------------------------
 
@@ -396,6 +422,7 @@ def pin_affine_beta_zero(oracle):
 ALL_PINS = [
     pin_eq1_exact_rational,
     pin_linear_attention,
+    pin_delta_rule_retrieval,
     pin_beta_zero_freeze,
     pin_recurrent_equals_chunkwise,
     pin_state_norm_bound,
